@@ -1,0 +1,454 @@
+// C ABI of the layer-end compressor: argument validation, scratch layout and
+// kernel launches.  Every check runs on the host before the first launch.
+#include <algorithm>
+#include <array>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+__device__ int g_status_word;
+
+namespace {
+thread_local char t_err[512] = "";
+int64_t g_opt_parts = 0;
+std::mutex g_mu;
+int g_sms[64] = {0};
+int* g_status_ptr[64] = {nullptr};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// stage timing (kvc_profile_begin / kvc_profile_end)
+std::atomic<int64_t> g_launch_count{0};
+bool g_prof = false;
+int64_t g_prof_launch_base = 0;
+std::vector<std::array<cudaEvent_t, KVC_N_STAGES + 1>> g_prof_ev;
+size_t g_prof_used = 0;
+}  // namespace
+
+void note_launches(int n) { g_launch_count += n; }
+
+// Next event set for a profiled call, or nullptr when not profiling.
+cudaEvent_t* prof_slot() {
+  if (!g_prof) return nullptr;
+  if (g_prof_used == g_prof_ev.size()) {
+    std::array<cudaEvent_t, KVC_N_STAGES + 1> ev{};
+    for (auto& e : ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_prof_ev.push_back(ev);
+  }
+  return g_prof_ev[g_prof_used++].data();
+}
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_error(cudaError_t e, const char* what) {
+  return set_error(KVC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+int* status_word_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int parts_per_head(int BH) {
+  if (g_opt_parts > 0) return (int)std::min<int64_t>(g_opt_parts, 1024);
+  const int sms = num_sms();
+  if (sms <= 0) return 0;
+  int p = (2 * sms + BH - 1) / BH;
+  return std::max(1, std::min(p, 512));
+}
+
+bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int pool_k,
+               WsLayout* L) {
+  (void)D;
+  (void)pool_k;
+  const int BH = B * H_kv;
+  const int np = parts_per_head(BH);
+  if (np <= 0) return false;
+  const int gw = (H_q / H_kv) * W;
+  L->nparts = np;
+  L->gwp = (gw + 15) / 16 * 16;
+  L->cap = std::max(K_l_max, 0) + b_s;
+  size_t o = 0;
+  L->off_part_m = o; o = align256(o + (size_t)BH * np * L->gwp * sizeof(float));
+  L->off_part_z = o; o = align256(o + (size_t)BH * np * L->gwp * sizeof(float));
+  L->off_hist = o;   o = align256(o + (size_t)BH * kHistPerSeg * sizeof(uint32_t));
+  L->off_pcnt = o;   o = align256(o + (size_t)BH * np * sizeof(int2));
+  L->off_cand_cnt = o; o = align256(o + (size_t)BH * np * sizeof(int));
+  L->off_cand = o;   o = align256(o + (size_t)BH * np * (size_t)L->cap * sizeof(uint64_t));
+  L->total = o;
+  return true;
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shapes(int B, int H_q, int H_kv, int S, int D, int W) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || S < 1 || W < 1)
+    return set_error(KVC_ERR_INVALID_ARG, "B, H_q, H_kv, S and W must be >= 1 (got B=%d H_q=%d H_kv=%d S=%d W=%d)", B, H_q, H_kv, S, W);
+  if (H_q % H_kv != 0)
+    return set_error(KVC_ERR_INVALID_ARG, "H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
+  if (W > S) return set_error(KVC_ERR_INVALID_ARG, "W (%d) must be <= S (%d)", W, S);
+  if (S > (1 << 30)) return set_error(KVC_ERR_UNSUPPORTED, "S (%d) above 2^30", S);
+  if (D != 64 && D != 128) return set_error(KVC_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are supported", D);
+  if (H_kv > kMaxHkv) return set_error(KVC_ERR_UNSUPPORTED, "H_kv=%d above %d", H_kv, kMaxHkv);
+  if ((H_q / H_kv) * W > kMaxGWP)
+    return set_error(KVC_ERR_UNSUPPORTED, "G*W=%d above %d window rows per KV head", (H_q / H_kv) * W, kMaxGWP);
+  return KVC_OK;
+}
+
+int check_bs(int b_s) {
+  if (b_s < kTile) return set_error(KVC_ERR_INVALID_ARG, "b_s=%d must be >= %d", b_s, kTile);
+  return KVC_OK;
+}
+
+int check_pool(int pool_k) {
+  if (pool_k < 1 || pool_k % 2 == 0) return set_error(KVC_ERR_INVALID_ARG, "pool_k=%d must be odd and >= 1", pool_k);
+  if (pool_k > kMaxPool) return set_error(KVC_ERR_UNSUPPORTED, "pool_k=%d above %d", pool_k, kMaxPool);
+  return KVC_OK;
+}
+
+int check_ptr(const void* p, size_t align, const char* name) {
+  if (!p) return set_error(KVC_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, align)) return set_error(KVC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+  return KVC_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return KVC_OK;
+  if (!ws) return set_error(KVC_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", need);
+  if (!aligned(ws, 256)) return set_error(KVC_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if (ws_bytes < need) return set_error(KVC_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  return KVC_OK;
+}
+
+// Selection parameters from the host budget array.
+int make_sel(int S, int H_kv, const int32_t* K_l, int sink, int recent, int nparts, SelParams* sp,
+             int* K_l_eff_max) {
+  if (!K_l) return set_error(KVC_ERR_INVALID_ARG, "K_l is NULL");
+  if (sink < 0 || recent < 0) return set_error(KVC_ERR_INVALID_ARG, "sink/recent must be >= 0");
+  std::memset(sp, 0, sizeof(*sp));
+  sp->S = S;
+  sp->sink = sink;
+  sp->recent = recent;
+  sp->H_kv = H_kv;
+  sp->nparts = nparts;
+  sp->r_lo = std::min(sink, S);
+  sp->r_hi = std::max(S - std::min(recent, S), sp->r_lo);
+  const int rsz = sp->r_lo + (S - sp->r_hi);
+  int64_t off = 0;
+  int mx = 0;
+  for (int h = 0; h < H_kv; ++h) {
+    if (K_l[h] < rsz)
+      return set_error(KVC_ERR_INVALID_ARG, "K_l[%d]=%d is smaller than the mandatory set (%d keys)", h, K_l[h], rsz);
+    const int kept = std::min(K_l[h], S);
+    sp->n_sel[h] = kept - rsz;
+    sp->off[h] = off;
+    off += kept;
+    mx = std::max(mx, kept);
+  }
+  sp->T = off;
+  if (K_l_eff_max) *K_l_eff_max = mx;
+  return KVC_OK;
+}
+
+int launch_status(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_error(e, what);
+  return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvc_last_error(void) { return t_err; }
+
+int kvc_version(void) { return 100; }
+
+int kvc_set_option(int option, int64_t value) {
+  if (option == KVC_OPT_PARTS_PER_HEAD) {
+    if (value < 0) return set_error(KVC_ERR_INVALID_ARG, "parts per head must be >= 0");
+    g_opt_parts = value;
+    return KVC_OK;
+  }
+  return set_error(KVC_ERR_INVALID_ARG, "unknown option %d", option);
+}
+
+size_t kvc_workspace_size(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int pool_k) {
+  // S is not an argument: use W as the smallest legal S for the shape checks.
+  if (check_shapes(B, H_q, H_kv, W, D, W) != KVC_OK) return 0;
+  if (check_bs(b_s) != KVC_OK || check_pool(pool_k) != KVC_OK) return 0;
+  if (K_l_max < 0) { set_error(KVC_ERR_INVALID_ARG, "K_l_max must be >= 0"); return 0; }
+  WsLayout L;
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, K_l_max, pool_k, &L)) {
+    set_error(KVC_ERR_CUDA, "no CUDA device to size the workspace for");
+    return 0;
+  }
+  return L.total;
+}
+
+int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, int H_kv, int S, int D,
+                    int W, int b_s, float* m, float* Z, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  int rc;
+  if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s))) return rc;
+  if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(m, 4, "m")) ||
+      (rc = check_ptr(Z, 4, "Z")))
+    return rc;
+  WsLayout L;
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, 0, 1, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  if ((rc = check_ws(ws, ws_bytes, L.off_part_z + (size_t)B * H_kv * L.nparts * L.gwp * 4))) return rc;
+  char* w = static_cast<char*>(ws);
+  float* pm = reinterpret_cast<float*>(w + L.off_part_m);
+  float* pz = reinterpret_cast<float*>(w + L.off_part_z);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
+  auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
+  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.nparts, L.gwp, pm, pz, st), "pass 1 launch")))
+    return rc;
+  return launch_status(launch_pass1_combine(pm, pz, B, H_q, H_kv, W, D, L.nparts, L.gwp, S, m, Z, st),
+                       "pass 1 combine launch");
+}
+
+int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* m, const float* Z, int B,
+                         int H_q, int H_kv, int S, int D, int W, int b_s, int pool_k, float* scores, void* ws,
+                         size_t ws_bytes, kvc_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  int rc;
+  if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s)) || (rc = check_pool(pool_k))) return rc;
+  if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(m, 4, "m")) ||
+      (rc = check_ptr(Z, 4, "Z")) || (rc = check_ptr(scores, 4, "scores")))
+    return rc;
+  const int BH = B * H_kv;
+  const int np = parts_per_head(BH);
+  if (np <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  const int gwp = ((H_q / H_kv) * W + 15) / 16 * 16;
+  SelParams sp{};
+  sp.S = S;
+  sp.H_kv = H_kv;
+  sp.nparts = np;
+  Pass2Out out{scores, nullptr, nullptr, 0, 0};
+  return launch_status(launch_pass2(reinterpret_cast<const __nv_bfloat16*>(q_win),
+                                    reinterpret_cast<const __nv_bfloat16*>(k), m, Z, nullptr, nullptr, B, H_q,
+                                    H_kv, S, D, W, pool_k, np, gwp, &sp, out,
+                                    reinterpret_cast<cudaStream_t>(stream)),
+                       "pass 2 launch");
+}
+
+int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* K_l, int sink, int recent,
+                    int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  int rc;
+  if (B < 1 || H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "B, H_kv and S must be >= 1");
+  if (H_kv > kMaxHkv) return set_error(KVC_ERR_UNSUPPORTED, "H_kv=%d above %d", H_kv, kMaxHkv);
+  if ((rc = check_ptr(scores, 4, "scores")) || (rc = check_ptr(idx, 4, "idx"))) return rc;
+  WsLayout L;
+  if (!layout_ws(B, H_kv, H_kv, 64, 1, kTile, 0, 1, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  SelParams sp;
+  if ((rc = make_sel(S, H_kv, K_l, sink, recent, L.nparts, &sp, nullptr))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L.off_pcnt + (size_t)B * H_kv * L.nparts * sizeof(int2)))) return rc;
+  char* w = static_cast<char*>(ws);
+  return launch_status(launch_select(0, scores, nullptr, nullptr, 0, B, sp,
+                                     reinterpret_cast<uint32_t*>(w + L.off_hist),
+                                     reinterpret_cast<int2*>(w + L.off_pcnt), idx,
+                                     reinterpret_cast<cudaStream_t>(stream)),
+                       "selection launch");
+}
+
+int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx, int B, int H_kv, int S, int D,
+               const int32_t* K_l, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, kvc_stream_t stream) {
+  int rc;
+  if (B < 1 || H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "B, H_kv and S must be >= 1");
+  if (D != 64 && D != 128) return set_error(KVC_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are supported", D);
+  if (H_kv > kMaxHkv) return set_error(KVC_ERR_UNSUPPORTED, "H_kv=%d above %d", H_kv, kMaxHkv);
+  if ((rc = check_ptr(k, 16, "k")) || (rc = check_ptr(v, 16, "v")) || (rc = check_ptr(idx, 4, "idx")) ||
+      (rc = check_ptr(k_out, 16, "k_out")) || (rc = check_ptr(v_out, 16, "v_out")) ||
+      (rc = check_ptr(pos_out, 4, "pos_out")))
+    return rc;
+  if (!K_l) return set_error(KVC_ERR_INVALID_ARG, "K_l is NULL");
+  std::vector<int64_t> off(H_kv + 1, 0);
+  for (int h = 0; h < H_kv; ++h) {
+    if (K_l[h] < 0) return set_error(KVC_ERR_INVALID_ARG, "K_l[%d]=%d is negative", h, K_l[h]);
+    off[h + 1] = off[h] + std::min(K_l[h], S);
+  }
+  return launch_status(launch_gather(reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v),
+                                     idx, B, H_kv, S, D, off[H_kv], off.data(), nullptr,
+                                     reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out),
+                                     pos_out, reinterpret_cast<cudaStream_t>(stream)),
+                       "gather launch");
+}
+
+int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int D, int W, const int32_t* K_l,
+                       int sink, int recent, int pool_k, int b_s, const kvc_bf16* q_win, const kvc_bf16* k,
+                       const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, void* ws,
+                       size_t ws_bytes, kvc_stream_t stream) {
+  int rc;
+  if (N < 1 || layer < 0 || layer >= N)
+    return set_error(KVC_ERR_INVALID_ARG, "layer %d outside [0, N=%d)", layer, N);
+  if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s)) || (rc = check_pool(pool_k))) return rc;
+  if (C < W || C > S) return set_error(KVC_ERR_INVALID_ARG, "chunk C=%d must satisfy W=%d <= C <= S=%d", C, W, S);
+  if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(v, 16, "v")) ||
+      (rc = check_ptr(k_out, 16, "k_out")) || (rc = check_ptr(v_out, 16, "v_out")) ||
+      (rc = check_ptr(pos_out, 4, "pos_out")))
+    return rc;
+  const int BH = B * H_kv;
+  const int np = parts_per_head(BH);
+  if (np <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  SelParams sp;
+  int kmax = 0;
+  if ((rc = make_sel(S, H_kv, K_l, sink, recent, np, &sp, &kmax))) return rc;
+  WsLayout L;
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, kmax, pool_k, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
+  char* w = static_cast<char*>(ws);
+  float* pm = reinterpret_cast<float*>(w + L.off_part_m);
+  float* pz = reinterpret_cast<float*>(w + L.off_part_z);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(w + L.off_cand);
+  int* cnt = reinterpret_cast<int*>(w + L.off_cand_cnt);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
+  auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
+  auto vv = reinterpret_cast<const __nv_bfloat16*>(v);
+  cudaEvent_t* ev = prof_slot();
+  if (ev) cudaEventRecord(ev[0], st);
+  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, np, L.gwp, pm, pz, st), "pass 1 launch")))
+    return rc;
+  if (ev) cudaEventRecord(ev[1], st);
+  Pass2Out out{nullptr, cand, cnt, L.cap, 0};
+  if ((rc = launch_status(launch_pass2(q, kk, nullptr, nullptr, pm, pz, B, H_q, H_kv, S, D, W, pool_k, np, L.gwp,
+                                       &sp, out, st),
+                          "pass 2 launch")))
+    return rc;
+  if (ev) cudaEventRecord(ev[2], st);
+  if ((rc = launch_status(launch_select(1, nullptr, cand, cnt, L.cap, B, sp, reinterpret_cast<uint32_t*>(w + L.off_hist),
+                                        reinterpret_cast<int2*>(w + L.off_pcnt), pos_out, st),
+                          "selection launch")))
+    return rc;
+  if (ev) cudaEventRecord(ev[3], st);
+  std::vector<int64_t> off(H_kv + 1);
+  for (int h = 0; h < H_kv; ++h) off[h] = sp.off[h];
+  off[H_kv] = sp.T;
+  rc = launch_status(launch_gather(kk, vv, pos_out, B, H_kv, S, D, sp.T, off.data(), nullptr,
+                                   reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out),
+                                   pos_out, st),
+                     "gather launch");
+  if (ev) cudaEventRecord(ev[4], st);
+  return rc;
+}
+
+int kvc_retained_layout(int H_kv, int S, const int32_t* K_l, int64_t* out_off) {
+  if (H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "H_kv and S must be >= 1");
+  if (!K_l || !out_off) return set_error(KVC_ERR_INVALID_ARG, "K_l and out_off must be non-NULL");
+  out_off[0] = 0;
+  for (int h = 0; h < H_kv; ++h) {
+    if (K_l[h] < 0) return set_error(KVC_ERR_INVALID_ARG, "K_l[%d] is negative", h);
+    out_off[h + 1] = out_off[h] + std::min(K_l[h], S);
+  }
+  return KVC_OK;
+}
+
+int kvc_budget_inverse_stability(int H_kv, const double* s_stable, int64_t total, int lo, int hi,
+                                 int32_t* K_l_out) {
+  if (H_kv < 1 || !s_stable || !K_l_out) return set_error(KVC_ERR_INVALID_ARG, "bad budget arguments");
+  if (total < 0 || lo < 0 || hi < lo) return set_error(KVC_ERR_INVALID_ARG, "need total >= 0 and 0 <= lo <= hi");
+  std::vector<double> w(H_kv), exact(H_kv), rem(H_kv);
+  double wsum = 0.0;
+  for (int h = 0; h < H_kv; ++h) {
+    if (!(s_stable[h] > 0.0)) return set_error(KVC_ERR_INVALID_ARG, "stability score %d must be > 0", h);
+    w[h] = 1.0 / s_stable[h];
+    wsum += w[h];
+  }
+  std::vector<int64_t> base(H_kv);
+  int64_t assigned = 0;
+  for (int h = 0; h < H_kv; ++h) {
+    exact[h] = (double)total * w[h] / wsum;
+    base[h] = (int64_t)std::floor(exact[h]);
+    rem[h] = exact[h] - (double)base[h];
+    assigned += base[h];
+  }
+  std::vector<int> order(H_kv);
+  for (int h = 0; h < H_kv; ++h) order[h] = h;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return rem[a] > rem[b]; });
+  for (int64_t i = 0; i < total - assigned && i < H_kv; ++i) base[order[i]] += 1;
+  for (int h = 0; h < H_kv; ++h) K_l_out[h] = (int32_t)std::min<int64_t>(std::max<int64_t>(base[h], lo), hi);
+  return KVC_OK;
+}
+
+int kvc_profile_begin(void) {
+  g_prof = true;
+  g_prof_used = 0;
+  g_prof_launch_base = g_launch_count.load();
+  return KVC_OK;
+}
+
+int kvc_profile_end(double* stage_ms, int64_t* calls, int64_t* launches) {
+  g_prof = false;
+  if (stage_ms)
+    for (int i = 0; i < KVC_N_STAGES; ++i) stage_ms[i] = 0.0;
+  if (calls) *calls = (int64_t)g_prof_used;
+  if (launches) *launches = g_launch_count.load() - g_prof_launch_base;
+  if (g_prof_used == 0) return KVC_OK;
+  cudaError_t e = cudaEventSynchronize(g_prof_ev[g_prof_used - 1][KVC_N_STAGES]);
+  if (e != cudaSuccess) return cuda_error(e, "profile event synchronize");
+  for (size_t c = 0; c < g_prof_used; ++c) {
+    for (int i = 0; i < KVC_N_STAGES; ++i) {
+      float ms = 0.f;
+      if ((e = cudaEventElapsedTime(&ms, g_prof_ev[c][i], g_prof_ev[c][i + 1])) != cudaSuccess)
+        return cuda_error(e, "profile elapsed time");
+      if (stage_ms) stage_ms[i] += ms;
+    }
+  }
+  return KVC_OK;
+}
+
+int kvc_check_status(kvc_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "stream synchronize");
+  int v = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int))) != cudaSuccess) return cuda_error(e, "status read");
+  const int zero = 0;
+  if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int))) != cudaSuccess) return cuda_error(e, "status clear");
+  if (v == kStatusOk) return KVC_OK;
+  if (v == kStatusTimeout) return set_error(KVC_ERR_TIMEOUT, "a device wait gave up");
+  return set_error(KVC_ERR_DEVICE, "kernel status %d (%s)", v,
+                   v == kStatusCandOverflow ? "candidate list overflow" : "selection count mismatch");
+}
+
+}  // extern "C"

@@ -1,0 +1,347 @@
+// Per-head top-k selection and gather (TideKV, Fig. 2 and Fig. 3).
+//
+// Selection keeps, per (b, KV head), the mandatory set R_mand = [0, sink) u
+// [S - recent, S) and the n_sel best other keys by (score desc, index asc),
+// listed in ascending position.  Scores are >= 0, so their fp32 bit patterns
+// order like the values; a three-round radix select over those bits (11, 11
+// and 10 bits, each round a histogram of the keys that share the digits found
+// so far) finds the n_sel-th score T and how many keys scoring exactly T are
+// still needed.  Ties at T are taken in ascending index order, which the last
+// two kernels resolve with per-range counts and an ordered block scan.
+//
+// The keys come either from a dense score array (mode 0) or from the
+// per-range candidate lists of the fused scorer (mode 1, entries
+// (score bits << 32 | index), ascending index within each range, ranges in
+// ascending key order).
+#include "kvc_device.cuh"
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kSelThreads = 256;
+
+struct SegView {
+  int mode;
+  const float* scores;     // mode 0: [BH][S]
+  const uint64_t* cand;    // mode 1: [BH][nparts][cap]
+  const int* cand_cnt;     // mode 1: [BH][nparts]
+  int cap;
+};
+
+// Number of entries and (score bits, index) of entry i of range `part` of
+// segment `seg`.
+__device__ __forceinline__ int range_len(const SegView& v, const SelParams& sp, int seg, int part,
+                                         int* first) {
+  if (v.mode == 0) {
+    const int ncand = sp.r_hi - sp.r_lo;
+    const int per = (ncand + sp.nparts - 1) / sp.nparts;
+    const int lo = part * per;
+    const int hi = min(ncand, lo + per);
+    *first = sp.r_lo + lo;
+    return max(0, hi - lo);
+  }
+  *first = 0;
+  return v.cand_cnt[(size_t)seg * sp.nparts + part];
+}
+
+__device__ __forceinline__ void entry_at(const SegView& v, const SelParams& sp, int seg, int part,
+                                         int first, int i, uint32_t* u, int* j) {
+  if (v.mode == 0) {
+    *j = first + i;
+    uint32_t bits = __float_as_uint(v.scores[(size_t)seg * sp.S + first + i]);
+    *u = (bits == 0x80000000u) ? 0u : bits;
+  } else {
+    const uint64_t e = v.cand[((size_t)seg * sp.nparts + part) * v.cap + i];
+    *u = (uint32_t)(e >> 32);
+    *j = (int)(uint32_t)e;
+  }
+}
+
+__device__ __forceinline__ int seg_total(const SegView& v, const SelParams& sp, int seg) {
+  if (v.mode == 0) return sp.r_hi - sp.r_lo;
+  int t = 0;
+  for (int p = 0; p < sp.nparts; ++p) t += v.cand_cnt[(size_t)seg * sp.nparts + p];
+  return t;
+}
+
+struct FindSmem {
+  int scan[32];
+  int digit, need;
+};
+
+// Given a histogram (nbins, digit d counts keys whose next digit is d) and the
+// number `need` of keys still to take among them, find the digit holding the
+// need-th largest key and how many keys of that digit are still needed.
+__device__ void find_digit(const uint32_t* hist, int nbins, int need, FindSmem* fs, int* digit_out,
+                           int* need_out) {
+  const int tid = threadIdx.x;
+  const int per = nbins / kSelThreads;   // 8 or 4 bins per thread, highest digits first
+  const int hi = nbins - 1 - tid * per;  // this thread covers digits hi, hi-1, ..., hi-per+1
+  if (tid == 0) { fs->digit = 0; fs->need = 0; }
+  int local = 0;
+  for (int i = 0; i < per; ++i) local += (int)hist[hi - i];
+  int tot;
+  const int incl = block_inclusive_scan(local, fs->scan, &tot);
+  const int before = incl - local;
+  if (before < need && need <= incl) {
+    int cum = before;
+    for (int i = 0; i < per; ++i) {
+      const int c = (int)hist[hi - i];
+      if (cum + c >= need) {
+        fs->digit = hi - i;
+        fs->need = need - cum;
+        break;
+      }
+      cum += c;
+    }
+  }
+  __syncthreads();
+  *digit_out = fs->digit;
+  *need_out = fs->need;
+  __syncthreads();
+}
+
+// Recompute the digits found by earlier rounds for segment `seg`.
+__device__ void replay_rounds(const uint32_t* hist_seg, int rounds, int n_sel, FindSmem* fs,
+                              uint32_t* prefix, int* need) {
+  uint32_t pre = 0;
+  int nd = n_sel, d;
+  if (rounds >= 1) { find_digit(hist_seg, kHist1, nd, fs, &d, &nd); pre = (uint32_t)d; }
+  if (rounds >= 2) { find_digit(hist_seg + kHist1, kHist2, nd, fs, &d, &nd); pre = (pre << 11) | (uint32_t)d; }
+  if (rounds >= 3) { find_digit(hist_seg + kHist1 + kHist2, kHist3, nd, fs, &d, &nd); pre = (pre << 10) | (uint32_t)d; }
+  *prefix = pre;
+  *need = nd;
+}
+
+// Histogram round `round` (0, 1, 2) over one key range.
+__global__ void __launch_bounds__(kSelThreads)
+hist_kernel(SegView v, const __grid_constant__ SelParams sp, int round, uint32_t* __restrict__ hist) {
+  const int part = blockIdx.x, seg = blockIdx.y, h = seg % sp.H_kv;
+  __shared__ uint32_t sh[kHist1];
+  __shared__ FindSmem fs;
+  const int n_sel = sp.n_sel[h];
+  const int total = seg_total(v, sp, seg);
+  if (n_sel <= 0 || n_sel >= total) return;  // nothing to rank
+  uint32_t* hseg = hist + (size_t)seg * kHistPerSeg;
+  uint32_t prefix = 0;
+  int need;
+  replay_rounds(hseg, round, n_sel, &fs, &prefix, &need);
+  const int nb = round == 2 ? kHist3 : kHist1;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  int first;
+  const int len = range_len(v, sp, seg, part, &first);
+  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+    uint32_t u;
+    int j;
+    entry_at(v, sp, seg, part, first, i, &u, &j);
+    if (round == 0) {
+      atomicAdd(&sh[u >> 21], 1u);
+    } else if (round == 1) {
+      if ((u >> 21) == prefix) atomicAdd(&sh[(u >> 10) & 2047u], 1u);
+    } else {
+      if ((u >> 10) == prefix) atomicAdd(&sh[u & 1023u], 1u);
+    }
+  }
+  __syncthreads();
+  uint32_t* dst = hseg + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
+  for (int i = threadIdx.x; i < nb; i += blockDim.x)
+    if (sh[i]) atomicAdd(&dst[i], sh[i]);
+}
+
+// Exact threshold T and the count of keys equal to T still needed.
+// take_all / take_none encode the trivial cases.
+__device__ void threshold(const SegView& v, const SelParams& sp, int seg, const uint32_t* hist,
+                          FindSmem* fs, uint32_t* T, int* need_eq, int* mode) {
+  const int h = seg % sp.H_kv;
+  const int n_sel = sp.n_sel[h];
+  const int total = seg_total(v, sp, seg);
+  if (n_sel <= 0) { *mode = 0; *T = 0; *need_eq = 0; return; }
+  if (n_sel >= total) { *mode = 2; *T = 0; *need_eq = 0; return; }
+  replay_rounds(hist + (size_t)seg * kHistPerSeg, 3, n_sel, fs, T, need_eq);
+  *mode = 1;
+}
+
+// Per range: number of keys scoring above T and exactly T.
+__global__ void __launch_bounds__(kSelThreads)
+count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
+             int2* __restrict__ pcnt) {
+  const int part = blockIdx.x, seg = blockIdx.y;
+  __shared__ FindSmem fs;
+  __shared__ int scan[32];
+  uint32_t T;
+  int need_eq, mode;
+  threshold(v, sp, seg, hist, &fs, &T, &need_eq, &mode);
+  int first;
+  const int len = range_len(v, sp, seg, part, &first);
+  int gt = 0, eq = 0;
+  if (mode == 1) {
+    for (int i = threadIdx.x; i < len; i += blockDim.x) {
+      uint32_t u;
+      int j;
+      entry_at(v, sp, seg, part, first, i, &u, &j);
+      gt += (u > T);
+      eq += (u == T);
+    }
+  } else if (mode == 2) {
+    gt = threadIdx.x == 0 ? len : 0;
+  }
+  int tg, te;
+  block_inclusive_scan(gt, scan, &tg);
+  block_inclusive_scan(eq, scan, &te);
+  if (threadIdx.x == 0) pcnt[(size_t)seg * sp.nparts + part] = make_int2(tg, te);
+}
+
+// Ordered write of the retained positions of one range; range 0 also writes
+// the mandatory positions.
+__global__ void __launch_bounds__(kSelThreads)
+write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
+             const int2* __restrict__ pcnt, int32_t* __restrict__ idx, int* status) {
+  const int part = blockIdx.x, seg = blockIdx.y;
+  const int b = seg / sp.H_kv, h = seg % sp.H_kv;
+  __shared__ FindSmem fs;
+  __shared__ int scan[32];
+  uint32_t T;
+  int need_eq, mode;
+  threshold(v, sp, seg, hist, &fs, &T, &need_eq, &mode);
+  const int n_sel = sp.n_sel[h];
+  const int n_take = mode == 0 ? 0 : mode == 2 ? seg_total(v, sp, seg) : n_sel;
+  int32_t* out = idx + (size_t)b * sp.T + sp.off[h];
+  if (part == 0) {
+    for (int jj = threadIdx.x; jj < sp.r_lo; jj += blockDim.x) out[jj] = jj;
+    for (int jj = sp.r_hi + threadIdx.x; jj < sp.S; jj += blockDim.x) out[sp.r_lo + n_take + (jj - sp.r_hi)] = jj;
+  }
+  if (mode == 0) return;
+  // exclusive prefix over earlier ranges; the ties taken by a range depend on
+  // the running tie count, so one thread walks them in order
+  int out_before = 0, eq_before = 0;
+  if (threadIdx.x == 0) {
+    int eqb = 0, ob = 0;
+    for (int q = 0; q < part; ++q) {
+      const int2 c = pcnt[(size_t)seg * sp.nparts + q];
+      const int take_eq = mode == 2 ? 0 : max(0, min(c.y, need_eq - eqb));
+      ob += c.x + take_eq;
+      eqb += c.y;
+    }
+    fs.digit = ob;
+    fs.need = eqb;
+  }
+  __syncthreads();
+  out_before = fs.digit;
+  eq_before = fs.need;
+  __syncthreads();
+  int first;
+  const int len = range_len(v, sp, seg, part, &first);
+  int written = 0, eq_seen = 0;
+  for (int base = 0; base < len; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    uint32_t u = 0;
+    int j = 0;
+    int is_eq = 0, is_gt = 0;
+    if (i < len) {
+      entry_at(v, sp, seg, part, first, i, &u, &j);
+      if (mode == 2) {
+        is_gt = 1;
+      } else {
+        is_gt = u > T;
+        is_eq = u == T;
+      }
+    }
+    int eq_tot;
+    const int eq_incl = block_inclusive_scan(is_eq, scan, &eq_tot);
+    const int eq_rank = eq_before + eq_seen + eq_incl - is_eq;
+    const int f = is_gt || (is_eq && eq_rank < need_eq);
+    int f_tot;
+    const int f_incl = block_inclusive_scan(f, scan, &f_tot);
+    if (f) {
+      const int r = out_before + written + f_incl - 1;
+      if (r < n_take) out[sp.r_lo + r] = j;
+      else record_status(status, kStatusSelectMismatch);
+    }
+    written += f_tot;
+    eq_seen += eq_tot;
+  }
+}
+
+// Gather retained rows: one 16-byte vector per lane, D/8 lanes per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+gather_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+              const int32_t* idx, const __grid_constant__ SelParams sp, int B,
+              __nv_bfloat16* __restrict__ k_out, __nv_bfloat16* __restrict__ v_out, int32_t* pos_out,
+              int* status) {
+  constexpr int LPR = D / 8;             // lanes per row
+  constexpr int RPW = 32 / LPR;          // rows per warp step
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, cl = lane % LPR;
+  const int64_t rows = (int64_t)B * sp.T;
+  const int64_t warp_g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = warp_g * RPW + sub; r < rows; r += nwarps * RPW) {
+    const int b = (int)(r / sp.T);
+    const int64_t within = r - (int64_t)b * sp.T;
+    int lo = 0, hi = sp.H_kv - 1;
+    while (lo < hi) {  // last head whose offset is <= within
+      const int mid = (lo + hi + 1) >> 1;
+      if (sp.off[mid] <= within) lo = mid; else hi = mid - 1;
+    }
+    const int j = idx[r];
+    if (j < 0 || j >= sp.S) {
+      if (cl == 0) record_status(status, kStatusSelectMismatch);
+      continue;
+    }
+    const size_t src = (((size_t)b * sp.H_kv + lo) * sp.S + j) * D + cl * 8;
+    const uint4 kv = *reinterpret_cast<const uint4*>(k + src);
+    const uint4 vv = *reinterpret_cast<const uint4*>(v + src);
+    *reinterpret_cast<uint4*>(k_out + (size_t)r * D + cl * 8) = kv;
+    *reinterpret_cast<uint4*>(v_out + (size_t)r * D + cl * 8) = vv;
+    if (cl == 0 && pos_out != idx) pos_out[r] = j;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt,
+                          int cap, int B, const SelParams& sel, uint32_t* hist, int2* pcnt,
+                          int32_t* idx, cudaStream_t st) {
+  SegView v{mode, scores, cand, cand_cnt, cap};
+  const int BH = B * sel.H_kv;
+  cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)BH * kHistPerSeg * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  dim3 grid(sel.nparts, BH);
+  for (int round = 0; round < 3; ++round) {
+    hist_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, round, hist);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  count_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  write_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt, idx, status_word_ptr());
+  note_launches(5);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* idx, int B,
+                          int H_kv, int S, int D, int64_t T, const int64_t* off_host,
+                          const int* kept_host, __nv_bfloat16* k_out, __nv_bfloat16* v_out,
+                          int32_t* pos_out, cudaStream_t st) {
+  (void)kept_host;
+  SelParams sp{};
+  sp.S = S;
+  sp.H_kv = H_kv;
+  sp.T = T;
+  for (int h = 0; h < H_kv; ++h) sp.off[h] = off_host[h];
+  const int64_t rows = (int64_t)B * T;
+  if (rows == 0) return cudaSuccess;
+  const int rows_per_block = (256 / 32) * (32 / (D / 8));
+  int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+  if (blocks > 4 * 1024) blocks = 4 * 1024;
+  if (D == 64)
+    gather_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
+  else
+    gather_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Layer-end compress benchmark on GB300.
+
+One step = one full layer-end compress (pass 1, pass 2 + pooling, per-head
+top-k, gather) of one layer of the chosen workload, through the C ABI
+(kvc_compress_layer).  Default workload: Mistral-7B layer shape at S=131072
+(B=1, H_q=32, H_kv=8, D=128, W=64, K_l=4096, sink 4, recent 64, avgpool 7,
+b_s 4096), seeded synthetic bf16 inputs drawn on the device.  Four distinct
+layers' inputs (512 MiB of K+V each) are cycled, so every step reads inputs
+larger than L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank compresses its own
+layers on its own GPU (independent replicas, no data-path collective).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "layer-end compress: prefix keys scored/s per KV head; HBM GB/s vs ~8 TB/s peak"
+UNIT = "prefix keys scored/s (per KV head)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default="mistral128k")
+    ap.add_argument("--layers", type=int, default=4, help="distinct layer inputs cycled")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(cfg):
+    kl = f"K_l={cfg.K_l}" if not cfg.inverse_stability else f"K_l~1/s, {cfg.budget_frac:.0%} of S*H_kv"
+    return (f"{cfg.name}: N={cfg.N} B={cfg.B} H_q={cfg.H_q} H_kv={cfg.H_kv} D={cfg.D} S={cfg.S} C={cfg.C} "
+            f"W={cfg.W} {kl} sink={cfg.sink} recent={cfg.recent} avgpool={cfg.pool_k} b_s={cfg.b_s} "
+            f"heavy_hitters={cfg.hh_frac:.0%}")
+
+
+def budgets(cfg, K, layer):
+    if not cfg.inverse_stability:
+        return [cfg.K_l] * cfg.H_kv
+    from synth import stability_scores
+    s = stability_scores(cfg, layer).numpy()
+    total = round(cfg.budget_frac * cfg.S * cfg.H_kv)
+    rsz = min(cfg.sink, cfg.S) + min(cfg.recent, max(cfg.S - cfg.sink, 0))
+    return K.kvc_budget_inverse_stability(s, total, rsz, cfg.S)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(cfg, inp_cpu, heads, budget_s):
+    """Time the CPU oracle on whole KV heads of one layer (bounded sample)."""
+    from oracle import kvc_oracle as O
+    K_l = [cfg.K_l if not cfg.inverse_stability else max(cfg.sink + cfg.recent, int(0.3 * cfg.S))] * cfg.H_kv
+    keys, t_used, done = 0, 0.0, []
+    for (b, h) in heads:
+        t0 = time.perf_counter()
+        O.compress_layer(inp_cpu["q"], inp_cpu["k"], inp_cpu["v"], K_l, cfg.sink, cfg.recent, cfg.pool_k,
+                         heads=[(b, h)])
+        t_used += time.perf_counter() - t0
+        keys += cfg.S
+        done.append((b, h))
+        if t_used >= budget_s:
+            break
+    return keys / t_used, t_used, done
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step a bounded sample (one KV
+    head over the first S_s keys of the workload's layer, taken as a prompt of
+    S_s keys)."""
+    import torch
+    from synth import get_config, make_layer_inputs
+    from oracle import kvc_oracle as O
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = get_config(args.config)
+    S_s = min(cfg.S, 8192)
+    budget_total = 150.0
+    inp = make_layer_inputs(cfg.with_(S=S_s, C=min(cfg.C, S_s)), 0)
+    q, k, v = inp.q_win, inp.k, inp.v
+    K_l = [min(cfg.K_l if not cfg.inverse_stability else int(0.3 * S_s), S_s)] * cfg.H_kv
+    K_l = [max(x, cfg.sink + cfg.recent) for x in K_l]
+
+    def step(i):
+        b, h = i % cfg.B, i % cfg.H_kv
+        O.compress_layer(q, k, v, K_l, cfg.sink, cfg.recent, cfg.pool_k, heads=[(b, h)])
+
+    t0 = time.perf_counter()
+    step(0)
+    t_one = time.perf_counter() - t0
+    while S_s > 512 and t_one * (args.steps + args.warmup) > budget_total:
+        S_s //= 2
+        inp = make_layer_inputs(cfg.with_(S=S_s, C=min(cfg.C, S_s), W=min(cfg.W, S_s)), 0)
+        q, k, v = inp.q_win, inp.k, inp.v
+        K_l = [max(min(x, S_s), cfg.sink + cfg.recent) for x in K_l]
+        t0 = time.perf_counter()
+        step(0)
+        t_one = time.perf_counter() - t0
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = args.steps * S_s / dt
+    sample = (f"one KV head per step (cycling b, h) of the first {S_s} keys of layer 0, dense fp64 "
+              f"softmax over G*W={cfg.GW} window rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(cfg), "sample_S": S_s},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from attention_score_kv_gb300 import build as _b
+    _b.build()
+    import attention_score_kv_gb300.kvc as K
+    from synth import get_config, make_layer_inputs
+
+    cfg = get_config(args.config)
+    NL = args.layers
+    layers = []
+    for l in range(NL):
+        layer_id = (rank * NL + l) % cfg.N
+        inp = make_layer_inputs(cfg, layer_id, device=dev)
+        kl = budgets(cfg, K, layer_id)
+        k_out, v_out, pos, off = K.retained_outputs(cfg.B, cfg.H_kv, cfg.S, cfg.D, kl, device=dev)
+        layers.append(dict(id=layer_id, q=inp.q_win, k=inp.k, v=inp.v, K_l=kl, k_out=k_out, v_out=v_out,
+                           pos=pos, T=off[-1]))
+    kmax = max(max(L["K_l"]) for L in layers)
+    ws = K.workspace(cfg.B, cfg.H_q, cfg.H_kv, cfg.D, cfg.W, cfg.b_s, kmax, cfg.pool_k, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        L = layers[i % NL]
+        K.kvc_compress_layer(cfg.N, L["id"], cfg.B, cfg.S, cfg.C, cfg.H_q, cfg.H_kv, cfg.D, cfg.W, L["K_l"],
+                             cfg.sink, cfg.recent, cfg.pool_k, cfg.b_s, L["q"], L["k"], L["v"], L["k_out"],
+                             L["v_out"], L["pos"], ws, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    K.kvc_check_status(stream)
+
+    # ---- timed region: device-resident inputs
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.15)
+    K.kvc_profile_begin()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    stage_ms, calls, launches = K.kvc_profile_end()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    K.kvc_check_status(stream)
+
+    units_per_step = cfg.B * cfg.H_kv * cfg.S
+    value = world * units_per_step * args.steps / (ms / 1e3)
+
+    # ---- roofline of the dominant kernel (algorithmic bytes per launch)
+    hbm_peak, _, peak_kind = load_peaks()
+    Tmean = sum(L["T"] for L in layers) / NL
+    kbytes = cfg.B * cfg.H_kv * cfg.S * cfg.D * 2
+    qbytes = cfg.B * cfg.H_q * cfg.W * cfg.D * 2
+    ncand = cfg.B * cfg.H_kv * max(0, cfg.S - cfg.sink - cfg.recent)
+    alg = {
+        "pass1": kbytes + qbytes,
+        "pass2_pool": kbytes + qbytes,
+        "select_topk": 5 * 8 * ncand + 4 * cfg.B * Tmean,
+        "gather": cfg.B * Tmean * (4 * cfg.D * 2 + 4),
+    }
+    names = K.STAGE_NAMES
+    per_launch_ms = [x / max(calls, 1) for x in stage_ms]
+    dom = max(range(len(names)), key=lambda i: per_launch_ms[i])
+    achieved = alg[names[dom]] / (per_launch_ms[dom] / 1e3) / 1e9
+    path_bytes = 2 * kbytes + 2 * qbytes + cfg.B * Tmean * (4 * cfg.D * 2 + 4)
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            tj = json.load(open(tfile))
+            ent = tj.get(args.config, {}).get(names[dom])
+            if ent and ent.get("source_digest") == _source_digest():
+                traffic = ent["bytes_per_launch"]
+        except (ValueError, KeyError):
+            traffic = None
+    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic, "peak_kind": peak_kind,
+                "alg_bytes_per_launch": alg[names[dom]], "ms_per_launch": per_launch_ms[dom]}
+    stages = {n: round(t, 5) for n, t in zip(names, per_launch_ms)}
+    path_gbs = path_bytes / (ms / args.steps / 1e3) / 1e9
+
+    # ---- end to end: host buffers, H2D + compress + D2H inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        nl_e = min(2, NL)
+        host = []
+        for L in layers[:nl_e]:
+            host.append(dict(q=L["q"].cpu().pin_memory(), k=L["k"].cpu().pin_memory(),
+                             v=L["v"].cpu().pin_memory(),
+                             ko=torch.empty(L["k_out"].shape, dtype=torch.bfloat16).pin_memory(),
+                             vo=torch.empty(L["v_out"].shape, dtype=torch.bfloat16).pin_memory(),
+                             po=torch.empty(L["pos"].shape, dtype=torch.int32).pin_memory()))
+        dq = torch.empty_like(layers[0]["q"])
+        dk = torch.empty_like(layers[0]["k"])
+        dv = torch.empty_like(layers[0]["v"])
+
+        def e2e_step(i):
+            H = host[i % nl_e]
+            L = layers[i % nl_e]
+            dq.copy_(H["q"], non_blocking=True)
+            dk.copy_(H["k"], non_blocking=True)
+            dv.copy_(H["v"], non_blocking=True)
+            K.kvc_compress_layer(cfg.N, L["id"], cfg.B, cfg.S, cfg.C, cfg.H_q, cfg.H_kv, cfg.D, cfg.W, L["K_l"],
+                                 cfg.sink, cfg.recent, cfg.pool_k, cfg.b_s, dq, dk, dv, L["k_out"], L["v_out"],
+                                 L["pos"], ws, stream=stream)
+            H["ko"].copy_(L["k_out"], non_blocking=True)
+            H["vo"].copy_(L["v_out"], non_blocking=True)
+            H["po"].copy_(L["pos"], non_blocking=True)
+
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = a0.elapsed_time(a1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        L0 = layers[0]
+        e2e = {"value": world * units_per_step * args.e2e_steps / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": (L0["q"].numel() + L0["k"].numel() + L0["v"].numel()) * 2,
+               "d2h_bytes_per_step": (L0["k_out"].numel() + L0["v_out"].numel()) * 2 + L0["pos"].numel() * 4,
+               "ms_per_step": ems / args.e2e_steps}
+        K.kvc_check_status(stream)
+
+    # ---- CPU baseline: the oracle on whole KV heads of layer 0 (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        L0 = layers[0]
+        heads = [(b, h) for b in range(cfg.B) for h in range(cfg.H_kv)]
+        inp_cpu = {"q": L0["q"].cpu(), "k": L0["k"].cpu(), "v": L0["v"].cpu()}
+        v_cpu, t_cpu, done = oracle_sample(cfg, inp_cpu, heads, args.cpu_seconds)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{len(done)} whole KV head(s) {done} of layer 0 ({cfg.S} keys each, dense fp64 "
+                         f"softmax over G*W={cfg.GW} rows), {t_cpu:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {NL} distinct layers of "
+                             f"{2 * kbytes / 2**20:.0f} MiB K+V cycled"},
+            "roofline": roofline,
+            "path_hbm_gbs": path_gbs, "path_alg_bytes_per_step": path_bytes,
+            "stage_ms_per_launch": stages,
+            "gpu_launches": launches, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_score_kv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    main()

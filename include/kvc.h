@@ -1,0 +1,199 @@
+/*
+ * kvc.h -- C ABI of the layer-end KV-cache compressor (GB300, sm_103a).
+ *
+ * The library scores every prefix key of a layer by how much attention the
+ * last W prompt positions (the observation window) pay to it, and keeps, per
+ * KV head, a fixed number of keys: the sink and recent keys plus the best
+ * scoring others.  It is TideKV's memory-controlled two-pass blockwise scorer
+ * ("TideKV: Delayed KV Eviction via Layer-Wise Chunked Prefill", Fig. 3),
+ * with unequal per-head budgets as in HeteroCache's inverse-stability
+ * allocation (HeteroCache summary, Phase 2).
+ *
+ * Notation (TideKV, Table 1): N layers, B batch, S prompt length, C prefill
+ * chunk, H_q query heads, H_kv KV heads, D head dim.  G = H_q / H_kv query
+ * heads share one KV head; query head g reads KV head g / G.  W is the
+ * observation window (window query i sits at absolute position
+ * t_i = S - W + i and attends to keys j <= t_i), b_s the key block of the
+ * scan, K_l the per-head budget, sink/recent the mandatory set
+ * R_mand = [0, sink) u [S - recent, S), pool_k the average-pool width.
+ *
+ * Conventions for every call
+ *  - Tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *    row-major in the shapes given; bf16 tensors are 16-byte aligned, fp32
+ *    and int32 tensors 4-byte aligned.  Budget arrays (K_l) and stability
+ *    scores are HOST arrays.
+ *  - The library allocates no device memory.  Scratch comes from the
+ *    caller's `ws` buffer of at least kvc_workspace_size(...) bytes (256-byte
+ *    aligned).  Its size does not depend on S.
+ *  - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *    return KVC_OK once the work is enqueued.  All arguments are validated on
+ *    the host before anything is launched; on error nothing is launched and
+ *    kvc_last_error() describes the problem.
+ *  - Kernels never trap.  A kernel that detects an inconsistency records a
+ *    code in a device status word; kvc_check_status() reads and clears it.
+ *  - Calls on one stream may run back to back; two calls that share a `ws`
+ *    buffer must not overlap on the GPU.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvc_bf16;                 /* raw bfloat16 bits */
+typedef struct CUstream_st* kvc_stream_t;  /* the same type as cudaStream_t */
+
+enum kvc_status_code {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = -1,  /* a size, pointer or budget breaks the contract */
+  KVC_ERR_UNSUPPORTED = -2,  /* valid, but outside what the kernels handle
+                                (D not 64/128, G*W > 256, pool_k > 15, H_kv > 128) */
+  KVC_ERR_WORKSPACE = -3,    /* ws missing, misaligned or too small */
+  KVC_ERR_CUDA = -4,         /* a CUDA runtime call failed (message has details) */
+  KVC_ERR_TIMEOUT = -5,      /* a bounded device wait gave up */
+  KVC_ERR_DEVICE = -6        /* a kernel recorded an inconsistency */
+};
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* kvc_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int kvc_version(void);
+
+/*
+ * Bytes of scratch every entry point below needs for these sizes on the
+ * current device.  There is no S argument: the scan keeps only W-length
+ * normaliser state per key range and, per key range, at most K_l_max + b_s
+ * candidate keys (TideKV Fig. 3: Temp = O(W b_s + K_l), independent of S).
+ * Returns 0 and sets kvc_last_error() on invalid sizes or without a device.
+ */
+size_t kvc_workspace_size(int B, int H_q, int H_kv, int D, int W, int b_s,
+                          int K_l_max, int pool_k);
+
+/*
+ * Pass 1 of the two-pass scorer (TideKV Fig. 3): scan the prefix keys block
+ * by block against the window queries and keep only the log-sum-exp
+ * normalisers of each window query.
+ *   q_win [B, H_q, W, D] bf16   the window queries (last W prompt positions)
+ *   k     [B, H_kv, S, D] bf16  the layer's prefix keys
+ *   m     [B, H_q, W] fp32 out  m = max_{j <= t_i} q.k_j / sqrt(D)
+ *   Z     [B, H_q, W] fp32 out  Z = sum_{j <= t_i} exp(q.k_j / sqrt(D) - m)
+ * b_s must be >= 128.
+ */
+int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q,
+                    int H_kv, int S, int D, int W, int b_s, float* m, float* Z,
+                    void* ws, size_t ws_bytes, kvc_stream_t stream);
+
+/*
+ * Pass 2 plus pooling (TideKV Fig. 3): rescan the keys, form the normalised
+ * weights exp(q.k/sqrt(D) - m) / Z, sum them over the window queries and the
+ * GQA group of each KV head (r_j), and average-pool r into per-key scores
+ *   s_j = (1/pool_k) * sum_{|d| <= (pool_k-1)/2} r_{j+d}   (r = 0 outside [0,S)).
+ *   m, Z    [B, H_q, W] fp32 from kvc_score_pass1
+ *   scores  [B, H_kv, S] fp32 out
+ * pool_k is odd, 1 <= pool_k <= 15 (1 = no pooling).
+ */
+int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k,
+                         const float* m, const float* Z, int B, int H_q,
+                         int H_kv, int S, int D, int W, int b_s, int pool_k,
+                         float* scores, void* ws, size_t ws_bytes,
+                         kvc_stream_t stream);
+
+/*
+ * Per-head selection (TideKV Fig. 3): keep R_mand and the top
+ * (K_l[h] - |R_mand|) other keys by (score descending, index ascending).
+ *   scores [B, H_kv, S] fp32 (>= 0)
+ *   K_l    HOST [H_kv]; K_l[h] >= |R_mand|.  A head with K_l[h] >= S keeps
+ *          every key.
+ *   idx    out, int32 positions, ascending within each head.  Head h of
+ *          batch element b occupies rows b * T + off[h] .. + min(K_l[h], S)
+ *          - 1, where off / T come from kvc_retained_layout.
+ */
+int kvc_select_topk(const float* scores, int B, int H_kv, int S,
+                    const int32_t* K_l, int sink, int recent, int32_t* idx,
+                    void* ws, size_t ws_bytes, kvc_stream_t stream);
+
+/*
+ * Gather of the retained cache (TideKV Fig. 2): copy K and V rows at the
+ * selected positions and record the positions.
+ *   k, v   [B, H_kv, S, D] bf16
+ *   idx    int32 positions in the layout of kvc_select_topk (values in [0,S))
+ *   k_out, v_out [B * T, D] bf16 out, pos_out [B * T] int32 out
+ * idx and pos_out may be the same buffer.
+ */
+int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx,
+               int B, int H_kv, int S, int D, const int32_t* K_l,
+               kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out,
+               kvc_stream_t stream);
+
+/*
+ * The whole layer-end compress of layer `layer` (TideKV Fig. 2 and 3):
+ * pass 1, pass 2 with pooling, selection, gather -- the step that runs once
+ * per layer after all of its prompt chunks, before the next layer starts.
+ * N, layer and C are the pages' symbols and are only validated:
+ * 0 <= layer < N and 1 <= W <= C <= S (the window is the tail of the last
+ * chunk); C does not change the result.  Outputs as kvc_gather.
+ * The per-head score vector is never materialised: each key range keeps a
+ * candidate list of at most K_l_max + b_s keys in `ws`.
+ */
+int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q,
+                       int H_kv, int D, int W, const int32_t* K_l, int sink,
+                       int recent, int pool_k, int b_s,
+                       const kvc_bf16* q_win, const kvc_bf16* k,
+                       const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out,
+                       int32_t* pos_out, void* ws, size_t ws_bytes,
+                       kvc_stream_t stream);
+
+/*
+ * Host helper: CSR layout of one batch element's retained rows.
+ * out_off HOST [H_kv + 1]: head h owns rows out_off[h] .. out_off[h+1]-1,
+ * with min(K_l[h], S) rows; out_off[H_kv] is the per-batch-element stride T.
+ */
+int kvc_retained_layout(int H_kv, int S, const int32_t* K_l, int64_t* out_off);
+
+/*
+ * Host helper (HeteroCache summary, Phase 2): per-KV-head budgets
+ * proportional to w_h = 1 / s_h.  The exact shares total * w_h / sum(w) are
+ * rounded by largest remainder (ties to the lower head index) so that they
+ * sum to `total`, then clamped to [lo, hi].  s_stable HOST [H_kv], > 0.
+ */
+int kvc_budget_inverse_stability(int H_kv, const double* s_stable,
+                                 int64_t total, int lo, int hi,
+                                 int32_t* K_l_out);
+
+/*
+ * Waits for `stream`, then reads and clears the device status word.
+ * Returns KVC_OK, or KVC_ERR_DEVICE / KVC_ERR_TIMEOUT with a message.
+ */
+int kvc_check_status(kvc_stream_t stream);
+
+/* Tuning knobs (process-wide, not thread-safe; 0 restores the default). */
+enum kvc_option {
+  KVC_OPT_PARTS_PER_HEAD = 1  /* key ranges per (b, KV head); default from the SM count */
+};
+int kvc_set_option(int option, int64_t value);
+
+/*
+ * Stage timing of kvc_compress_layer, for measurement.  Between
+ * kvc_profile_begin() and kvc_profile_end() every kvc_compress_layer call
+ * records CUDA events on its own stream around its stages (0 pass 1,
+ * 1 pass 2 + pooling + candidate lists, 2 selection, 3 gather).
+ * kvc_profile_end waits for the last recorded event and returns, per stage,
+ * the device time summed over the recorded calls (stage_ms[KVC_N_STAGES]),
+ * the number of calls and the number of kernels (and memsets) the library
+ * launched meanwhile.  Events are created once and reused; process-wide,
+ * not thread-safe.
+ */
+#define KVC_N_STAGES 4
+int kvc_profile_begin(void);
+int kvc_profile_end(double* stage_ms, int64_t* calls, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

@@ -282,18 +282,21 @@ def budgets_inverse_stability(s_stable, total: int, lo: int, hi: int) -> np.ndar
     rounded by largest remainder (ties to the lower head index) so that they
     sum to ``total``, then clamped to [lo, hi] without redistribution.
     """
-    s = np.asarray(s_stable, dtype=np.float64)
-    if np.any(s <= 0):
+    s = [float(x) for x in np.asarray(s_stable, dtype=np.float64)]
+    if any(x <= 0 for x in s):
         raise ValueError("stability scores must be > 0")
-    w = 1.0 / s
-    exact = total * w / w.sum()
-    base = np.floor(exact).astype(np.int64)
-    short = int(total - base.sum())
-    rem = exact - base
+    w = [1.0 / x for x in s]
+    wsum = 0.0
+    for x in w:                      # plain left-to-right sum, in head order
+        wsum += x
+    exact = [total * x / wsum for x in w]
+    base = [math.floor(x) for x in exact]
+    short = int(total - sum(base))
+    rem = [x - b for x, b in zip(exact, base)]
     order = sorted(range(len(s)), key=lambda i: (-rem[i], i))
     for i in order[:short]:
         base[i] += 1
-    return np.clip(base, lo, hi).astype(np.int32)
+    return np.clip(np.array(base, dtype=np.int64), lo, hi).astype(np.int32)
 
 
 def retained_layout(S: int, K_l) -> np.ndarray:

@@ -1,0 +1,153 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-only
+logic (validation, budgets, layout) behaves as specified.  No GPU work."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as O
+from synth import get_config, stability_scores
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvc.h")
+
+
+@pytest.fixture(scope="module")
+def K():
+    from attention_score_kv_gb300 import build
+    build.build()
+    import attention_score_kv_gb300.kvc as kvc
+    return kvc
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("kvc_score_pass1", "kvc_score_pass2_pool", "kvc_select_topk", "kvc_gather",
+                 "kvc_compress_layer", "kvc_workspace_size"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(K):
+    lib = ctypes.CDLL(K.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in kvc.h but not exported"
+        assert name in K.EXPORTED, f"{name} has no Python binding"
+
+
+def test_workspace_size_has_no_S_argument():
+    src = open(HEADER).read()
+    m = re.search(r"size_t kvc_workspace_size\(([^)]*)\)", src, flags=re.S)
+    args = [a.strip().split()[-1] for a in m.group(1).split(",")]
+    assert "S" not in args
+    assert args == ["B", "H_q", "H_kv", "D", "W", "b_s", "K_l_max", "pool_k"]
+
+
+def test_version(K):
+    assert K.kvc_version() == 100
+
+
+def _call_compress(K, **over):
+    a = dict(N=1, layer=0, B=1, S=512, C=512, H_q=4, H_kv=2, D=64, W=16, K_l=[128, 128], sink=4,
+             recent=16, pool_k=1, b_s=128, q_win=0x1000, k=0x2000, v=0x3000, k_out=0x4000,
+             v_out=0x5000, pos_out=0x6000, ws=0x10000, ws_bytes=1 << 30, stream=0)
+    a.update(over)
+    return K.kvc_compress_layer(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H_q=5), -1),                 # H_q % H_kv != 0
+    (dict(W=600, C=600), -1),          # W > S
+    (dict(D=96), -2),                  # unsupported head dim
+    (dict(layer=1), -1),               # layer >= N
+    (dict(C=8), -1),                   # C < W
+    (dict(C=1024), -1),                # C > S
+    (dict(pool_k=4), -1),              # even pool
+    (dict(pool_k=17), -2),             # pool wider than supported
+    (dict(b_s=64), -1),                # block smaller than the scan tile
+    (dict(q_win=0), -1),               # null pointer
+    (dict(k=0x2004), -1),              # misaligned bf16 tensor
+    (dict(H_q=64, H_kv=2, W=16), -2),  # G*W = 512 > 256
+])
+def test_compress_layer_rejects_bad_arguments(K, over, code):
+    with pytest.raises(K.KvcError) as ei:
+        _call_compress(K, **over)
+    assert ei.value.code == code
+
+
+def test_budget_below_mandatory_set_is_rejected_before_launch(K):
+    # |R_mand| = 4 + 16 = 20 > 19; checked on the host (no device needed to fail)
+    with pytest.raises(K.KvcError) as ei:
+        K.kvc_select_topk(0x1000, 1, 2, 512, [19, 128], 4, 16, 0x2000, 0x10000, 1 << 20, stream=0)
+    assert ei.value.code in (-1, -4)
+
+
+def test_select_null_scores(K):
+    with pytest.raises(K.KvcError) as ei:
+        K.kvc_select_topk(0, 1, 2, 512, [128, 128], 4, 16, 0x2000, 0x10000, 1 << 20, stream=0)
+    assert ei.value.code == -1
+
+
+def test_budgets_match_oracle_bit_exact(K):
+    cfg = get_config("qwen14b")
+    total = round(cfg.budget_frac * cfg.S * cfg.H_kv)
+    rsz = cfg.sink + cfg.recent
+    for layer in range(48):
+        s = stability_scores(cfg, layer).numpy()
+        got = K.kvc_budget_inverse_stability(s, total, rsz, cfg.S)
+        exp = O.budgets_inverse_stability(s, total, rsz, cfg.S)
+        assert got == exp.tolist()
+        assert sum(got) == total
+    # clamp and tie cases
+    assert K.kvc_budget_inverse_stability([1.0, 1.0, 0.01], 300, 50, 200) == \
+        O.budgets_inverse_stability([1.0, 1.0, 0.01], 300, 50, 200).tolist()
+    assert K.kvc_budget_inverse_stability([1.0] * 3, 10, 0, 100) == [4, 3, 3]
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        H = int(rng.integers(1, 17))
+        s = rng.uniform(0.01, 1.0, H)
+        total = int(rng.integers(0, 100000))
+        assert K.kvc_budget_inverse_stability(s, total, 0, 1 << 30) == \
+            O.budgets_inverse_stability(s, total, 0, 1 << 30).tolist()
+
+
+def test_retained_layout_matches_oracle(K):
+    for S, kl in [(100, [10, 200, 5]), (512, [128, 128]), (32768, [4096] * 8)]:
+        assert K.kvc_retained_layout(len(kl), S, kl) == O.retained_layout(S, kl).tolist()
+
+
+def test_main_config_retained_cache_is_512_mib(K):
+    cfg = get_config("tidekv_main")
+    off = K.kvc_retained_layout(cfg.H_kv, cfg.S, [cfg.K_l] * cfg.H_kv)
+    per_layer = off[-1] * cfg.B * cfg.D * 2 * 2      # K and V, bf16
+    assert per_layer * cfg.N == 512 * 2**20
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """Importing the binding with no libkvc.so raises instead of falling back."""
+    import importlib.util
+    src = os.path.join(ROOT, "attention_score_kv_gb300", "kvc.py")
+    dst = tmp_path / "kvc.py"
+    dst.write_text(open(src).read())
+    spec = importlib.util.spec_from_file_location("kvc_copy", dst)
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)
+
+
+def test_product_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "attention_score_kv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in re.sub(r"(#|//).*", "", txt), f"{f} mentions the oracle"
