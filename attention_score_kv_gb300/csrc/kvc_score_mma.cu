@@ -57,7 +57,7 @@ __device__ __forceinline__ float2 merge_mz(float2 a, float2 b) {
 // ------------------------------------------------------------------ pass 1
 template <int D, int KS>
 __global__ void __launch_bounds__(kThreads)
-pass1_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+kvc_pass1_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              int H_q, int H_kv, int S, int W, int nparts, int gwp, float c2,
              float* __restrict__ part_m, float* __restrict__ part_z) {
   constexpr int NT = 16 / KS;      // 8-key MMA tiles per work unit
@@ -175,7 +175,7 @@ pass1_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
 }
 
 // Combine the per-range partials of pass 1 into m, Z (natural-log units).
-__global__ void pass1_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_z,
+__global__ void kvc_pass1_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_z,
                                      int H_q, int H_kv, int W, int nparts, int gwp,
                                      float* __restrict__ m, float* __restrict__ Z) {
   const int bh = blockIdx.x;
@@ -267,7 +267,7 @@ __device__ void cta_compact(uint64_t* buf, int cnt, int n_keep, CompactSmem* cs,
 // ------------------------------------------------------------------ pass 2
 template <int D, bool CAND>
 __global__ void __launch_bounds__(kThreads)
-pass2_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+kvc_pass2_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const float* __restrict__ m, const float* __restrict__ Z,
              const float* __restrict__ part_m, const float* __restrict__ part_z,
              int H_q, int H_kv, int S, int W, int pool_k, int nparts, int gwp, float c2,
@@ -449,9 +449,9 @@ template <int D, int KS>
 cudaError_t run_pass1(dim3 grid, size_t smem, cudaStream_t st, const __nv_bfloat16* q,
                       const __nv_bfloat16* k, int H_q, int H_kv, int S, int W, int nparts,
                       int gwp, float c2, float* pm, float* pz) {
-  cudaError_t e = cudaFuncSetAttribute(pass1_kernel<D, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kvc_pass1_kernel<D, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  pass1_kernel<D, KS><<<grid, kThreads, smem, st>>>(q, k, H_q, H_kv, S, W, nparts, gwp, c2, pm, pz);
+  kvc_pass1_kernel<D, KS><<<grid, kThreads, smem, st>>>(q, k, H_q, H_kv, S, W, nparts, gwp, c2, pm, pz);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -473,9 +473,9 @@ cudaError_t run_pass2(dim3 grid, size_t smem, cudaStream_t st, const __nv_bfloat
                       const __nv_bfloat16* k, const float* m, const float* Z, const float* pm,
                       const float* pz, int H_q, int H_kv, int S, int W, int pool_k, int nparts,
                       int gwp, float c2, const SelParams* sel, Pass2Out out) {
-  cudaError_t e = cudaFuncSetAttribute(pass2_kernel<D, CAND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(kvc_pass2_kernel<D, CAND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  pass2_kernel<D, CAND><<<grid, kThreads, smem, st>>>(q, k, m, Z, pm, pz, H_q, H_kv, S, W, pool_k, nparts, gwp,
+  kvc_pass2_kernel<D, CAND><<<grid, kThreads, smem, st>>>(q, k, m, Z, pm, pz, H_q, H_kv, S, W, pool_k, nparts, gwp,
                                                        c2, out.scores, out.cand, out.cand_cnt, out.cap, *sel,
                                                        status_word_ptr());
   note_launches(1);
@@ -503,7 +503,7 @@ cudaError_t launch_pass1_combine(const float* part_m, const float* part_z, int B
                                  cudaStream_t st) {
   (void)D;
   (void)S;
-  pass1_combine_kernel<<<B * H_kv, 256, 0, st>>>(part_m, part_z, H_q, H_kv, W, nparts, gwp, m, Z);
+  kvc_pass1_combine_kernel<<<B * H_kv, 256, 0, st>>>(part_m, part_z, H_q, H_kv, W, nparts, gwp, m, Z);
   note_launches(1);
   return cudaGetLastError();
 }

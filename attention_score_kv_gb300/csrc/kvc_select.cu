@@ -116,7 +116,7 @@ __device__ void replay_rounds(const uint32_t* hist_seg, int rounds, int n_sel, F
 
 // Histogram round `round` (0, 1, 2) over one key range.
 __global__ void __launch_bounds__(kSelThreads)
-hist_kernel(SegView v, const __grid_constant__ SelParams sp, int round, uint32_t* __restrict__ hist) {
+kvc_hist_kernel(SegView v, const __grid_constant__ SelParams sp, int round, uint32_t* __restrict__ hist) {
   const int part = blockIdx.x, seg = blockIdx.y, h = seg % sp.H_kv;
   __shared__ uint32_t sh[kHist1];
   __shared__ FindSmem fs;
@@ -165,7 +165,7 @@ __device__ void threshold(const SegView& v, const SelParams& sp, int seg, const 
 
 // Per range: number of keys scoring above T and exactly T.
 __global__ void __launch_bounds__(kSelThreads)
-count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
+kvc_count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
              int2* __restrict__ pcnt) {
   const int part = blockIdx.x, seg = blockIdx.y;
   __shared__ FindSmem fs;
@@ -196,7 +196,7 @@ count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __
 // Ordered write of the retained positions of one range; range 0 also writes
 // the mandatory positions.
 __global__ void __launch_bounds__(kSelThreads)
-write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
+kvc_write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
              const int2* __restrict__ pcnt, int32_t* __restrict__ idx, int* status) {
   const int part = blockIdx.x, seg = blockIdx.y;
   const int b = seg / sp.H_kv, h = seg % sp.H_kv;
@@ -267,7 +267,7 @@ write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __
 // Gather retained rows: one 16-byte vector per lane, D/8 lanes per row.
 template <int D>
 __global__ void __launch_bounds__(256)
-gather_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+kvc_gather_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
               const int32_t* idx, const __grid_constant__ SelParams sp, int B,
               __nv_bfloat16* __restrict__ k_out, __nv_bfloat16* __restrict__ v_out, int32_t* pos_out,
               int* status) {
@@ -311,12 +311,12 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   if (e != cudaSuccess) return e;
   dim3 grid(sel.nparts, BH);
   for (int round = 0; round < 3; ++round) {
-    hist_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, round, hist);
+    kvc_hist_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, round, hist);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  count_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt);
+  kvc_count_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  write_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt, idx, status_word_ptr());
+  kvc_write_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt, idx, status_word_ptr());
   note_launches(5);
   return cudaGetLastError();
 }
@@ -337,9 +337,9 @@ cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const 
   int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
   if (blocks > 4 * 1024) blocks = 4 * 1024;
   if (D == 64)
-    gather_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
+    kvc_gather_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
   else
-    gather_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
+    kvc_gather_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
   note_launches(1);
   return cudaGetLastError();
 }
