@@ -1,0 +1,104 @@
+// Pass 1 of the scorer for callers that cannot allocate device memory.
+//
+// kvc_score_pass1 takes its scratch (the per-key-range partial normalisers)
+// from a caller-provided workspace.  Some callers cannot provide one: code
+// running inside a host framework that owns all device memory through its
+// own pool (a cudaMalloc there fails or breaks the pool's accounting), and
+// plugin or real-time paths that are not allowed to call the CUDA allocator
+// at all, since cudaMalloc/cudaFree may synchronise the whole device.  For
+// them this entry point keeps the scratch in a fixed array in the library's
+// own device memory and allocates nothing.
+//
+// The array lives for as long as the library is loaded, on every GPU that
+// loads it (1 MiB each).  All calls share it: two calls whose kernels overlap
+// on the GPU (on different streams, or from different host threads) race on
+// it and must be serialised by the caller.  Nothing in it needs to start at
+// zero: pass 1 writes every partial it later reads.
+#include <algorithm>
+#include <mutex>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;   // 1 MiB per device
+constexpr size_t kNoAllocScratchFloats = kNoAllocScratchBytes / sizeof(float);
+
+static __device__ __align__(256) float g_pass1_noalloc_scratch[kNoAllocScratchFloats];
+
+std::mutex g_na_mu;
+float* g_na_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+int scratch_on_current_device(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(KVC_ERR_UNSUPPORTED, "device ordinal %d above 63", dev);
+  std::lock_guard<std::mutex> lk(g_na_mu);
+  if (!g_na_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pass1_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress of the pass-1 scratch array");
+    g_na_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_na_ptr[dev];
+  return KVC_OK;
+}
+
+bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" int kvc_score_pass1_noalloc(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, int H_kv,
+                                       int S, int D, int W, int b_s, float* m, float* Z,
+                                       kvc_stream_t stream) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || S < 1 || W < 1)
+    return set_error(KVC_ERR_INVALID_ARG, "B, H_q, H_kv, S and W must be >= 1");
+  if (H_q % H_kv != 0) return set_error(KVC_ERR_INVALID_ARG, "H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
+  if (W > S) return set_error(KVC_ERR_INVALID_ARG, "W (%d) must be <= S (%d)", W, S);
+  if (S > (1 << 30)) return set_error(KVC_ERR_UNSUPPORTED, "S (%d) above 2^30", S);
+  if (D != 64 && D != 128) return set_error(KVC_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are supported", D);
+  if ((H_q / H_kv) * W > kMaxGWP)
+    return set_error(KVC_ERR_UNSUPPORTED, "G*W=%d above %d window rows per KV head", (H_q / H_kv) * W, kMaxGWP);
+  if (b_s < kTile) return set_error(KVC_ERR_INVALID_ARG, "b_s=%d must be >= %d", b_s, kTile);
+  if (!q_win || !k || !m || !Z) return set_error(KVC_ERR_INVALID_ARG, "q_win, k, m and Z must be non-NULL");
+  if (!is_aligned(q_win, 16) || !is_aligned(k, 16)) return set_error(KVC_ERR_INVALID_ARG, "q_win and k must be 16-byte aligned");
+  if (!is_aligned(m, 4) || !is_aligned(Z, 4)) return set_error(KVC_ERR_INVALID_ARG, "m and Z must be 4-byte aligned");
+
+  // Partials need 2 * gwp floats per (b, KV head, key range); fit the number
+  // of key ranges to the fixed array, and refuse shapes where even one range
+  // per head does not fit.
+  const int64_t BH = (int64_t)B * H_kv;
+  const int gwp = ((H_q / H_kv) * W + 15) / 16 * 16;
+  const int64_t per_range = BH * gwp * 2;
+  if (per_range > (int64_t)kNoAllocScratchFloats)
+    return set_error(KVC_ERR_UNSUPPORTED,
+                     "B*H_kv*G*W too large for the allocation-free pass 1: needs %lld bytes of scratch, "
+                     "the fixed array holds %zu",
+                     (long long)(per_range * (int64_t)sizeof(float)), kNoAllocScratchBytes);
+  int np = parts_per_head((int)BH);
+  if (np <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  np = (int)std::min<int64_t>(np, (int64_t)kNoAllocScratchFloats / per_range);
+  np = std::max(np, 1);
+
+  float* scratch = nullptr;
+  int rc = scratch_on_current_device(&scratch);
+  if (rc != KVC_OK) return rc;
+  float* pm = scratch;
+  float* pz = scratch + BH * np * gwp;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
+  auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
+  cudaError_t e = launch_pass1(q, kk, B, H_q, H_kv, S, D, W, np, gwp, pm, pz, st);
+  if (e != cudaSuccess) return cuda_error(e, "allocation-free pass 1 launch");
+  e = launch_pass1_combine(pm, pz, B, H_q, H_kv, W, D, np, gwp, S, m, Z, st);
+  if (e != cudaSuccess) return cuda_error(e, "allocation-free pass 1 combine launch");
+  return KVC_OK;
+}

@@ -58,6 +58,7 @@ _SIGS = {
     "kvc_version": (_I, []),
     "kvc_workspace_size": (_SZ, [_I] * 8),
     "kvc_score_pass1": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "kvc_score_pass1_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_score_pass2_pool": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvc_select_topk": (_I, [_P, _I, _I, _I, _I32P, _I, _I, _P, _P, _SZ, _P]),
     "kvc_gather": (_I, [_P, _P, _P, _I, _I, _I, _I, _I32P, _P, _P, _P, _P]),
@@ -124,6 +125,13 @@ def kvc_workspace_size(B, H_q, H_kv, D, W, b_s, K_l_max, pool_k) -> int:
 def kvc_score_pass1(q_win, k, B, H_q, H_kv, S, D, W, b_s, m, Z, ws, ws_bytes=None, stream=None):
     _check(_lib.kvc_score_pass1(_ptr(q_win), _ptr(k), B, H_q, H_kv, S, D, W, b_s, _ptr(m), _ptr(Z),
                                 _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def kvc_score_pass1_noalloc(q_win, k, B, H_q, H_kv, S, D, W, b_s, m, Z, stream=None):
+    """Pass 1 with the library's fixed scratch array instead of a workspace,
+    for callers that may not allocate device memory (see include/kvc.h)."""
+    _check(_lib.kvc_score_pass1_noalloc(_ptr(q_win), _ptr(k), B, H_q, H_kv, S, D, W, b_s, _ptr(m), _ptr(Z),
+                                        _stream(stream)))
 
 
 def kvc_score_pass2_pool(q_win, k, m, Z, B, H_q, H_kv, S, D, W, b_s, pool_k, scores, ws=None,

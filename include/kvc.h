@@ -89,6 +89,28 @@ int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q,
                     void* ws, size_t ws_bytes, kvc_stream_t stream);
 
 /*
+ * kvc_score_pass1 without a workspace, for callers that cannot allocate
+ * device memory: code inside a framework that owns all device memory through
+ * its own pool (a cudaMalloc there fails or breaks the pool's accounting),
+ * and plugin or real-time paths that may not call the CUDA allocator, whose
+ * cudaMalloc/cudaFree can synchronise the whole device.  The pages have no
+ * counterpart of this call; it only changes where the scratch lives.
+ *
+ * Same arguments and results as kvc_score_pass1, minus ws.  The scratch is a
+ * fixed 1 MiB array in the library's device memory, present on every GPU
+ * that loads the library until the process exits; nothing is allocated.
+ * Shapes with B * H_kv * roundup16(G*W) * 8 bytes above 1 MiB are rejected
+ * with KVC_ERR_UNSUPPORTED before any launch.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Every
+ * call shares the array: calls whose kernels could overlap on the GPU race
+ * and must be serialised by the caller.
+ */
+int kvc_score_pass1_noalloc(const kvc_bf16* q_win, const kvc_bf16* k, int B,
+                            int H_q, int H_kv, int S, int D, int W, int b_s,
+                            float* m, float* Z, kvc_stream_t stream);
+
+/*
  * Pass 2 plus pooling (TideKV Fig. 3): rescan the keys, form the normalised
  * weights exp(q.k/sqrt(D) - m) / Z, sum them over the window queries and the
  * GQA group of each KV head (r_j), and average-pool r into per-key scores
