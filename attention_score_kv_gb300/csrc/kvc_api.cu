@@ -1,5 +1,6 @@
-// C ABI of the layer-end compressor: argument validation, scratch layout and
-// kernel launches.  Every check runs on the host before the first launch.
+// C ABI of the layer-end compressor: argument validation, scan plan, scratch
+// layout and kernel launches.  Every check runs on the host before the first
+// launch.
 #include <algorithm>
 #include <array>
 #include <atomic>
@@ -18,7 +19,7 @@ __device__ int g_status_word;
 
 namespace {
 thread_local char t_err[512] = "";
-int64_t g_opt_parts = 0;
+int64_t g_opt_scan_ctas = 0;
 std::mutex g_mu;
 int g_sms[64] = {0};
 int* g_status_ptr[64] = {nullptr};
@@ -31,6 +32,8 @@ bool g_prof = false;
 int64_t g_prof_launch_base = 0;
 std::vector<std::array<cudaEvent_t, KVC_N_STAGES + 1>> g_prof_ev;
 size_t g_prof_used = 0;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 }  // namespace
 
 void note_launches(int n) { g_launch_count += n; }
@@ -83,32 +86,69 @@ int* status_word_ptr() {
   return g_status_ptr[dev];
 }
 
-int parts_per_head(int BH) {
-  if (g_opt_parts > 0) return (int)std::min<int64_t>(g_opt_parts, 1024);
-  const int sms = num_sms();
-  if (sms <= 0) return 0;
-  int p = (2 * sms + BH - 1) / BH;
-  return std::max(1, std::min(p, 512));
+int scan_ctas_target() {
+  if (g_opt_scan_ctas > 0) return (int)std::min<int64_t>(g_opt_scan_ctas, 1 << 16);
+  return num_sms();
 }
 
-bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int pool_k,
-               WsLayout* L) {
+ScanPlan plan_for(int BH, int S, int P) {
+  const int64_t total = (int64_t)BH * S;
+  int64_t p = std::max<int64_t>(1, std::min<int64_t>(P, total));
+  const int64_t L = ceil_div(total, p);
+  p = ceil_div(total, L);
+  ScanPlan pl;
+  pl.P = (int)p;
+  pl.L = L;
+  int maxseg = 1;
+  for (int64_t c = 0; c < p; ++c) {
+    const int64_t f0 = c * L, f1 = std::min(f0 + L, total);
+    maxseg = std::max<int>(maxseg, (int)((f1 - 1) / S - f0 / S + 1));
+  }
+  int nparts = 1;
+  for (int64_t h = 0; h < BH; ++h)
+    nparts = std::max<int>(nparts, (int)(((h + 1) * S - 1) / L - (h * S) / L + 1));
+  pl.maxseg = maxseg;
+  pl.nparts = nparts;
+  return pl;
+}
+
+ScanPlan make_plan(int BH, int S) {
+  const int64_t total = (int64_t)BH * S;
+  int64_t P = scan_ctas_target();
+  if (g_opt_scan_ctas <= 0) P = std::min<int64_t>(P, ceil_div(total, kMinKeysPerCta));
+  P = std::max<int64_t>(P, ceil_div(BH, kMaxSeg - 2));
+  return plan_for(BH, S, (int)std::max<int64_t>(P, 1));
+}
+
+static int max_ctas(int BH) {
+  return std::max<int>(std::max(scan_ctas_target(), 1), (int)ceil_div(BH, kMaxSeg - 2));
+}
+int max_slots(int BH) { return BH + 3 * max_ctas(BH); }
+int max_parts(int BH) { return max_ctas(BH); }
+
+bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int pool_k, int S, WsLayout* L) {
   (void)D;
   (void)pool_k;
+  if (num_sms() <= 0) return false;
   const int BH = B * H_kv;
-  const int np = parts_per_head(BH);
-  if (np <= 0) return false;
   const int gw = (H_q / H_kv) * W;
-  L->nparts = np;
+  if (S > 0) {
+    L->plan = make_plan(BH, S);
+    L->slots = L->plan.P * L->plan.maxseg;
+  } else {
+    L->plan = ScanPlan{0, 0, 0, 0};
+    L->slots = max_slots(BH);
+  }
+  const int parts = max_parts(BH);
   L->gwp = (gw + 15) / 16 * 16;
   L->cap = std::max(K_l_max, 0) + b_s;
   size_t o = 0;
-  L->off_part_m = o; o = align256(o + (size_t)BH * np * L->gwp * sizeof(float));
-  L->off_part_z = o; o = align256(o + (size_t)BH * np * L->gwp * sizeof(float));
-  L->off_hist = o;   o = align256(o + (size_t)BH * kHistPerSeg * sizeof(uint32_t));
-  L->off_pcnt = o;   o = align256(o + (size_t)BH * np * sizeof(int2));
-  L->off_cand_cnt = o; o = align256(o + (size_t)BH * np * sizeof(int));
-  L->off_cand = o;   o = align256(o + (size_t)BH * np * (size_t)L->cap * sizeof(uint64_t));
+  L->off_part_m = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
+  L->off_part_z = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
+  L->off_hist = o;     o = align256(o + (size_t)BH * kHistPerSeg * sizeof(uint32_t));
+  L->off_pcnt = o;     o = align256(o + (size_t)BH * parts * sizeof(int2));
+  L->off_cand_cnt = o; o = align256(o + (size_t)L->slots * sizeof(int));
+  L->off_cand = o;     o = align256(o + (size_t)L->slots * (size_t)L->cap * sizeof(uint64_t));
   L->total = o;
   return true;
 }
@@ -123,15 +163,17 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int check_shapes(int B, int H_q, int H_kv, int S, int D, int W) {
   if (B < 1 || H_q < 1 || H_kv < 1 || S < 1 || W < 1)
-    return set_error(KVC_ERR_INVALID_ARG, "B, H_q, H_kv, S and W must be >= 1 (got B=%d H_q=%d H_kv=%d S=%d W=%d)", B, H_q, H_kv, S, W);
-  if (H_q % H_kv != 0)
-    return set_error(KVC_ERR_INVALID_ARG, "H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
+    return set_error(KVC_ERR_INVALID_ARG, "B, H_q, H_kv, S and W must be >= 1 (got B=%d H_q=%d H_kv=%d S=%d W=%d)", B,
+                     H_q, H_kv, S, W);
+  if (H_q % H_kv != 0) return set_error(KVC_ERR_INVALID_ARG, "H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
   if (W > S) return set_error(KVC_ERR_INVALID_ARG, "W (%d) must be <= S (%d)", W, S);
   if (S > (1 << 30)) return set_error(KVC_ERR_UNSUPPORTED, "S (%d) above 2^30", S);
   if (D != 64 && D != 128) return set_error(KVC_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are supported", D);
   if (H_kv > kMaxHkv) return set_error(KVC_ERR_UNSUPPORTED, "H_kv=%d above %d", H_kv, kMaxHkv);
   if ((H_q / H_kv) * W > kMaxGWP)
     return set_error(KVC_ERR_UNSUPPORTED, "G*W=%d above %d window rows per KV head", (H_q / H_kv) * W, kMaxGWP);
+  if ((int64_t)B * H_q * W > (1LL << 31) || (int64_t)B * H_kv > (1LL << 24))
+    return set_error(KVC_ERR_UNSUPPORTED, "batch too large");
   return KVC_OK;
 }
 
@@ -161,8 +203,7 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
 }
 
 // Selection parameters from the host budget array.
-int make_sel(int S, int H_kv, const int32_t* K_l, int sink, int recent, int nparts, SelParams* sp,
-             int* K_l_eff_max) {
+int make_sel(int S, int H_kv, const int32_t* K_l, int sink, int recent, SelParams* sp, int* K_l_eff_max) {
   if (!K_l) return set_error(KVC_ERR_INVALID_ARG, "K_l is NULL");
   if (sink < 0 || recent < 0) return set_error(KVC_ERR_INVALID_ARG, "sink/recent must be >= 0");
   std::memset(sp, 0, sizeof(*sp));
@@ -170,7 +211,7 @@ int make_sel(int S, int H_kv, const int32_t* K_l, int sink, int recent, int npar
   sp->sink = sink;
   sp->recent = recent;
   sp->H_kv = H_kv;
-  sp->nparts = nparts;
+  sp->nparts = 1;
   sp->r_lo = std::min(sink, S);
   sp->r_hi = std::max(S - std::min(recent, S), sp->r_lo);
   const int rsz = sp->r_lo + (S - sp->r_hi);
@@ -201,12 +242,12 @@ extern "C" {
 
 const char* kvc_last_error(void) { return t_err; }
 
-int kvc_version(void) { return 100; }
+int kvc_version(void) { return 200; }
 
 int kvc_set_option(int option, int64_t value) {
-  if (option == KVC_OPT_PARTS_PER_HEAD) {
-    if (value < 0) return set_error(KVC_ERR_INVALID_ARG, "parts per head must be >= 0");
-    g_opt_parts = value;
+  if (option == KVC_OPT_SCAN_CTAS) {
+    if (value < 0) return set_error(KVC_ERR_INVALID_ARG, "scan CTA count must be >= 0");
+    g_opt_scan_ctas = value;
     return KVC_OK;
   }
   return set_error(KVC_ERR_INVALID_ARG, "unknown option %d", option);
@@ -216,39 +257,42 @@ size_t kvc_workspace_size(int B, int H_q, int H_kv, int D, int W, int b_s, int K
   // S is not an argument: use W as the smallest legal S for the shape checks.
   if (check_shapes(B, H_q, H_kv, W, D, W) != KVC_OK) return 0;
   if (check_bs(b_s) != KVC_OK || check_pool(pool_k) != KVC_OK) return 0;
-  if (K_l_max < 0) { set_error(KVC_ERR_INVALID_ARG, "K_l_max must be >= 0"); return 0; }
+  if (K_l_max < 0) {
+    set_error(KVC_ERR_INVALID_ARG, "K_l_max must be >= 0");
+    return 0;
+  }
   WsLayout L;
-  if (!layout_ws(B, H_q, H_kv, D, W, b_s, K_l_max, pool_k, &L)) {
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, K_l_max, pool_k, -1, &L)) {
     set_error(KVC_ERR_CUDA, "no CUDA device to size the workspace for");
     return 0;
   }
   return L.total;
 }
 
-int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, int H_kv, int S, int D,
-                    int W, int b_s, float* m, float* Z, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, int H_kv, int S, int D, int W,
+                    int b_s, float* m, float* Z, void* ws, size_t ws_bytes, kvc_stream_t stream) {
   int rc;
   if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s))) return rc;
   if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(m, 4, "m")) ||
       (rc = check_ptr(Z, 4, "Z")))
     return rc;
   WsLayout L;
-  if (!layout_ws(B, H_q, H_kv, D, W, b_s, 0, 1, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
-  if ((rc = check_ws(ws, ws_bytes, L.off_part_z + (size_t)B * H_kv * L.nparts * L.gwp * 4))) return rc;
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, 0, 1, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  if ((rc = check_ws(ws, ws_bytes, L.off_part_z + (size_t)L.slots * L.gwp * sizeof(float)))) return rc;
   char* w = static_cast<char*>(ws);
   float* pm = reinterpret_cast<float*>(w + L.off_part_m);
   float* pz = reinterpret_cast<float*>(w + L.off_part_z);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
   auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
-  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.nparts, L.gwp, pm, pz, st), "pass 1 launch")))
+  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, st), "pass 1 launch")))
     return rc;
-  return launch_status(launch_pass1_combine(pm, pz, B, H_q, H_kv, W, D, L.nparts, L.gwp, S, m, Z, st),
+  return launch_status(launch_pass1_combine(pm, pz, B, H_q, H_kv, S, W, L.plan, L.gwp, m, Z, st),
                        "pass 1 combine launch");
 }
 
-int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* m, const float* Z, int B,
-                         int H_q, int H_kv, int S, int D, int W, int b_s, int pool_k, float* scores, void* ws,
+int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* m, const float* Z, int B, int H_q,
+                         int H_kv, int S, int D, int W, int b_s, int pool_k, float* scores, void* ws,
                          size_t ws_bytes, kvc_stream_t stream) {
   (void)ws;
   (void)ws_bytes;
@@ -257,19 +301,16 @@ int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* 
   if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(m, 4, "m")) ||
       (rc = check_ptr(Z, 4, "Z")) || (rc = check_ptr(scores, 4, "scores")))
     return rc;
-  const int BH = B * H_kv;
-  const int np = parts_per_head(BH);
-  if (np <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  if (num_sms() <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  const ScanPlan pl = make_plan(B * H_kv, S);
   const int gwp = ((H_q / H_kv) * W + 15) / 16 * 16;
   SelParams sp{};
   sp.S = S;
   sp.H_kv = H_kv;
-  sp.nparts = np;
-  Pass2Out out{scores, nullptr, nullptr, 0, 0};
+  Pass2Out out{scores, nullptr, nullptr, 0};
   return launch_status(launch_pass2(reinterpret_cast<const __nv_bfloat16*>(q_win),
-                                    reinterpret_cast<const __nv_bfloat16*>(k), m, Z, nullptr, nullptr, B, H_q,
-                                    H_kv, S, D, W, pool_k, np, gwp, &sp, out,
-                                    reinterpret_cast<cudaStream_t>(stream)),
+                                    reinterpret_cast<const __nv_bfloat16*>(k), m, Z, nullptr, nullptr, B, H_q, H_kv,
+                                    S, D, W, pool_k, pl, gwp, &sp, out, reinterpret_cast<cudaStream_t>(stream)),
                        "pass 2 launch");
 }
 
@@ -279,14 +320,15 @@ int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* 
   if (B < 1 || H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "B, H_kv and S must be >= 1");
   if (H_kv > kMaxHkv) return set_error(KVC_ERR_UNSUPPORTED, "H_kv=%d above %d", H_kv, kMaxHkv);
   if ((rc = check_ptr(scores, 4, "scores")) || (rc = check_ptr(idx, 4, "idx"))) return rc;
-  WsLayout L;
-  if (!layout_ws(B, H_kv, H_kv, 64, 1, kTile, 0, 1, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
   SelParams sp;
-  if ((rc = make_sel(S, H_kv, K_l, sink, recent, L.nparts, &sp, nullptr))) return rc;
-  if ((rc = check_ws(ws, ws_bytes, L.off_pcnt + (size_t)B * H_kv * L.nparts * sizeof(int2)))) return rc;
+  if ((rc = make_sel(S, H_kv, K_l, sink, recent, &sp, nullptr))) return rc;
+  WsLayout L;
+  if (!layout_ws(B, H_kv, H_kv, 64, 1, kTile, 0, 1, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  const int BH = B * H_kv;
+  sp.nparts = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(2 * (int64_t)num_sms(), BH), max_parts(BH)));
+  if ((rc = check_ws(ws, ws_bytes, L.off_pcnt + (size_t)BH * max_parts(BH) * sizeof(int2)))) return rc;
   char* w = static_cast<char*>(ws);
-  return launch_status(launch_select(0, scores, nullptr, nullptr, 0, B, sp,
-                                     reinterpret_cast<uint32_t*>(w + L.off_hist),
+  return launch_status(launch_select(0, scores, nullptr, nullptr, 0, B, sp, reinterpret_cast<uint32_t*>(w + L.off_hist),
                                      reinterpret_cast<int2*>(w + L.off_pcnt), idx,
                                      reinterpret_cast<cudaStream_t>(stream)),
                        "selection launch");
@@ -308,11 +350,11 @@ int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx, int B, 
     if (K_l[h] < 0) return set_error(KVC_ERR_INVALID_ARG, "K_l[%d]=%d is negative", h, K_l[h]);
     off[h + 1] = off[h] + std::min(K_l[h], S);
   }
-  return launch_status(launch_gather(reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v),
-                                     idx, B, H_kv, S, D, off[H_kv], off.data(), nullptr,
-                                     reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out),
-                                     pos_out, reinterpret_cast<cudaStream_t>(stream)),
-                       "gather launch");
+  return launch_status(
+      launch_gather(reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), idx, B, H_kv,
+                    S, D, off[H_kv], off.data(), reinterpret_cast<__nv_bfloat16*>(k_out),
+                    reinterpret_cast<__nv_bfloat16*>(v_out), pos_out, reinterpret_cast<cudaStream_t>(stream)),
+      "gather launch");
 }
 
 int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int D, int W, const int32_t* K_l,
@@ -320,23 +362,22 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
                        const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, void* ws,
                        size_t ws_bytes, kvc_stream_t stream) {
   int rc;
-  if (N < 1 || layer < 0 || layer >= N)
-    return set_error(KVC_ERR_INVALID_ARG, "layer %d outside [0, N=%d)", layer, N);
+  if (N < 1 || layer < 0 || layer >= N) return set_error(KVC_ERR_INVALID_ARG, "layer %d outside [0, N=%d)", layer, N);
   if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s)) || (rc = check_pool(pool_k))) return rc;
   if (C < W || C > S) return set_error(KVC_ERR_INVALID_ARG, "chunk C=%d must satisfy W=%d <= C <= S=%d", C, W, S);
   if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(v, 16, "v")) ||
       (rc = check_ptr(k_out, 16, "k_out")) || (rc = check_ptr(v_out, 16, "v_out")) ||
       (rc = check_ptr(pos_out, 4, "pos_out")))
     return rc;
-  const int BH = B * H_kv;
-  const int np = parts_per_head(BH);
-  if (np <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
   SelParams sp;
   int kmax = 0;
-  if ((rc = make_sel(S, H_kv, K_l, sink, recent, np, &sp, &kmax))) return rc;
+  if ((rc = make_sel(S, H_kv, K_l, sink, recent, &sp, &kmax))) return rc;
   WsLayout L;
-  if (!layout_ws(B, H_q, H_kv, D, W, b_s, kmax, pool_k, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, kmax, pool_k, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
   if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
+  sp.nparts = L.plan.nparts;
+  sp.L = L.plan.L;
+  sp.maxseg = L.plan.maxseg;
   char* w = static_cast<char*>(ws);
   float* pm = reinterpret_cast<float*>(w + L.off_part_m);
   float* pz = reinterpret_cast<float*>(w + L.off_part_z);
@@ -348,13 +389,13 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
   auto vv = reinterpret_cast<const __nv_bfloat16*>(v);
   cudaEvent_t* ev = prof_slot();
   if (ev) cudaEventRecord(ev[0], st);
-  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, np, L.gwp, pm, pz, st), "pass 1 launch")))
+  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, st), "pass 1 launch")))
     return rc;
   if (ev) cudaEventRecord(ev[1], st);
-  Pass2Out out{nullptr, cand, cnt, L.cap, 0};
-  if ((rc = launch_status(launch_pass2(q, kk, nullptr, nullptr, pm, pz, B, H_q, H_kv, S, D, W, pool_k, np, L.gwp,
-                                       &sp, out, st),
-                          "pass 2 launch")))
+  Pass2Out out{nullptr, cand, cnt, L.cap};
+  if ((rc = launch_status(
+           launch_pass2(q, kk, nullptr, nullptr, pm, pz, B, H_q, H_kv, S, D, W, pool_k, L.plan, L.gwp, &sp, out, st),
+           "pass 2 launch")))
     return rc;
   if (ev) cudaEventRecord(ev[2], st);
   if ((rc = launch_status(launch_select(1, nullptr, cand, cnt, L.cap, B, sp, reinterpret_cast<uint32_t*>(w + L.off_hist),
@@ -365,7 +406,7 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
   std::vector<int64_t> off(H_kv + 1);
   for (int h = 0; h < H_kv; ++h) off[h] = sp.off[h];
   off[H_kv] = sp.T;
-  rc = launch_status(launch_gather(kk, vv, pos_out, B, H_kv, S, D, sp.T, off.data(), nullptr,
+  rc = launch_status(launch_gather(kk, vv, pos_out, B, H_kv, S, D, sp.T, off.data(),
                                    reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out),
                                    pos_out, st),
                      "gather launch");
@@ -384,8 +425,7 @@ int kvc_retained_layout(int H_kv, int S, const int32_t* K_l, int64_t* out_off) {
   return KVC_OK;
 }
 
-int kvc_budget_inverse_stability(int H_kv, const double* s_stable, int64_t total, int lo, int hi,
-                                 int32_t* K_l_out) {
+int kvc_budget_inverse_stability(int H_kv, const double* s_stable, int64_t total, int lo, int hi, int32_t* K_l_out) {
   if (H_kv < 1 || !s_stable || !K_l_out) return set_error(KVC_ERR_INVALID_ARG, "bad budget arguments");
   if (total < 0 || lo < 0 || hi < lo) return set_error(KVC_ERR_INVALID_ARG, "need total >= 0 and 0 <= lo <= hi");
   std::vector<double> w(H_kv), exact(H_kv), rem(H_kv);

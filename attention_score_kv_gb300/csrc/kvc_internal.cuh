@@ -10,10 +10,12 @@
 namespace kvc {
 
 // ---------------------------------------------------------------- limits
-constexpr int kTile = 128;          // keys per scan tile (MMA N / M extent)
+constexpr int kTile = 128;          // keys per scan tile (MMA M or N extent)
 constexpr int kMaxHkv = 128;        // KV heads per call (selection params live in the kernel argument block)
 constexpr int kMaxGWP = 256;        // G*W rounded up to 16
 constexpr int kMaxPool = 15;        // widest average pool
+constexpr int kMaxSeg = 8;          // KV heads one scan CTA may touch
+constexpr int kMinKeysPerCta = 1024;
 constexpr int kHist1 = 2048;        // radix digits: bits 31..21, 20..10, 9..0 of the score
 constexpr int kHist2 = 2048;
 constexpr int kHist3 = 1024;
@@ -25,16 +27,28 @@ constexpr int kStatusCandOverflow = 1;
 constexpr int kStatusSelectMismatch = 2;
 constexpr int kStatusTimeout = 3;
 
+// How the flattened key space [B*H_kv][S] is cut into scan CTAs: CTA c owns
+// keys [c*L, (c+1)*L) and touches at most `maxseg` KV heads; one head is
+// touched by at most `nparts` CTAs.  Per-(CTA, head) "slots" hold pass-1
+// partials and pass-2 candidate lists: slot = c * maxseg + (head - first head of c).
+struct ScanPlan {
+  int P;
+  int64_t L;
+  int maxseg;
+  int nparts;
+};
+
 // Scratch layout inside the caller's workspace (all offsets 256-aligned).
 struct WsLayout {
-  int nparts;      // key ranges per (b, KV head)
+  ScanPlan plan;
+  int slots;       // partial / candidate slots reserved
   int gwp;         // G*W rounded up to 16
-  int cap;         // candidate capacity per key range (K_l_max + b_s)
-  size_t off_part_m, off_part_z;   // float [BH][nparts][gwp]
-  size_t off_cand;                 // uint64 [BH][nparts][cap]
-  size_t off_cand_cnt;             // int    [BH][nparts]
+  int cap;         // candidate capacity per slot (K_l_max + b_s)
+  size_t off_part_m, off_part_z;   // float  [slots][gwp]
   size_t off_hist;                 // uint32 [BH][kHistPerSeg]
-  size_t off_pcnt;                 // int2   [BH][nparts]
+  size_t off_pcnt;                 // int2   [BH][plan.nparts]
+  size_t off_cand_cnt;             // int    [slots]
+  size_t off_cand;                 // uint64 [slots][cap]
   size_t total;
 };
 
@@ -44,6 +58,8 @@ struct SelParams {
   int r_lo;             // min(sink, S): mandatory keys at the front
   int r_hi;             // max(S - recent, r_lo): first mandatory key at the back
   int64_t T;            // retained rows per batch element
+  int64_t L;            // scan plan (candidate-list mode)
+  int maxseg;
   int n_sel[kMaxHkv];   // non-mandatory keys kept per head (or all candidates)
   int64_t off[kMaxHkv]; // row offset of head h inside a batch element
 };
@@ -52,47 +68,40 @@ struct SelParams {
 int set_error(int code, const char* fmt, ...);
 int cuda_error(cudaError_t e, const char* what);
 int num_sms();
-int parts_per_head(int BH);
-bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max,
-               int pool_k, WsLayout* L);
+int scan_ctas_target();                             // SM count or the tuning override
+ScanPlan plan_for(int BH, int S, int P);            // exact plan for P CTAs
+ScanPlan make_plan(int BH, int S);                  // default plan
+int max_slots(int BH);                              // S-independent bound on plan slots
+int max_parts(int BH);                              // S-independent bound on plan.nparts
+bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int pool_k, int S,
+               WsLayout* L);                        // S < 0: the S-independent upper bound
 
 // --------------------------------------------------------- kernel launchers
-// pass 1: per key range partial normalisers (raw-dot max, Z relative to it)
-cudaError_t launch_pass1(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                         int B, int H_q, int H_kv, int S, int D, int W,
-                         int nparts, int gwp, float* part_m, float* part_z,
-                         cudaStream_t st);
-cudaError_t launch_pass1_combine(const float* part_m, const float* part_z,
-                                 int B, int H_q, int H_kv, int W, int D,
-                                 int nparts, int gwp, int S, float* m, float* Z,
-                                 cudaStream_t st);
+// pass 1: per-slot partial normalisers (log2-domain max, Z relative to it)
+cudaError_t launch_pass1(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S, int D,
+                         int W, const ScanPlan& pl, int gwp, float* part_m, float* part_z, cudaStream_t st);
+cudaError_t launch_pass1_combine(const float* part_m, const float* part_z, int B, int H_q, int H_kv, int S,
+                                 int W, const ScanPlan& pl, int gwp, float* m, float* Z, cudaStream_t st);
 // pass 2: lse from (m, Z) (natural units) or from pass-1 partials; output
-// either dense scores or per-range candidate lists
+// either dense scores or per-slot candidate lists
 struct Pass2Out {
   float* scores;          // dense [BH][S] or nullptr
-  uint64_t* cand;         // [BH][nparts][cap] or nullptr
-  int* cand_cnt;          // [BH][nparts]
+  uint64_t* cand;         // [slots][cap] or nullptr
+  int* cand_cnt;          // [slots]
   int cap;
-  int n_sel_max_any;      // unused by kernels; kept for symmetry
 };
-cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                         const float* m, const float* Z,
-                         const float* part_m, const float* part_z,
-                         int B, int H_q, int H_kv, int S, int D, int W,
-                         int pool_k, int nparts, int gwp,
-                         const SelParams* sel, Pass2Out out, cudaStream_t st);
+cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const float* m, const float* Z,
+                         const float* part_m, const float* part_z, int B, int H_q, int H_kv, int S, int D, int W,
+                         int pool_k, const ScanPlan& pl, int gwp, const SelParams* sel, Pass2Out out,
+                         cudaStream_t st);
 // selection over dense scores (mode 0) or candidate lists (mode 1)
-cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand,
-                          const int* cand_cnt, int cap, int B,
-                          const SelParams& sel, uint32_t* hist, int2* pcnt,
-                          int32_t* idx, cudaStream_t st);
-cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v,
-                          const int32_t* idx, int B, int H_kv, int S, int D,
-                          int64_t T, const int64_t* off_host, const int* kept_host,
-                          __nv_bfloat16* k_out, __nv_bfloat16* v_out,
-                          int32_t* pos_out, cudaStream_t st);
+cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt, int cap, int B,
+                          const SelParams& sel, uint32_t* hist, int2* pcnt, int32_t* idx, cudaStream_t st);
+cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* idx, int B, int H_kv,
+                          int S, int D, int64_t T, const int64_t* off_host, __nv_bfloat16* k_out,
+                          __nv_bfloat16* v_out, int32_t* pos_out, cudaStream_t st);
 
-int* status_word_ptr();   // device address of the status word
-void note_launches(int n); // count kernels/memsets issued (measurement)
+int* status_word_ptr();     // device address of the status word
+void note_launches(int n);  // count kernels issued (measurement)
 
 }  // namespace kvc

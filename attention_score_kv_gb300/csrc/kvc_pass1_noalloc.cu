@@ -72,33 +72,34 @@ extern "C" int kvc_score_pass1_noalloc(const kvc_bf16* q_win, const kvc_bf16* k,
   if (!is_aligned(q_win, 16) || !is_aligned(k, 16)) return set_error(KVC_ERR_INVALID_ARG, "q_win and k must be 16-byte aligned");
   if (!is_aligned(m, 4) || !is_aligned(Z, 4)) return set_error(KVC_ERR_INVALID_ARG, "m and Z must be 4-byte aligned");
 
-  // Partials need 2 * gwp floats per (b, KV head, key range); fit the number
-  // of key ranges to the fixed array, and refuse shapes where even one range
-  // per head does not fit.
-  const int64_t BH = (int64_t)B * H_kv;
+  // Partials need 2 * gwp floats per (scan CTA, KV head it touches).  Use the
+  // default scan plan when its partials fit the fixed array, else one CTA per
+  // head (one slot per head); refuse shapes where even that does not fit.
+  if ((int64_t)B * H_kv > (1LL << 24)) return set_error(KVC_ERR_UNSUPPORTED, "batch too large");
+  const int BH = B * H_kv;
   const int gwp = ((H_q / H_kv) * W + 15) / 16 * 16;
-  const int64_t per_range = BH * gwp * 2;
-  if (per_range > (int64_t)kNoAllocScratchFloats)
+  const int64_t per_slot = (int64_t)gwp * 2;
+  if ((int64_t)BH * per_slot > (int64_t)kNoAllocScratchFloats)
     return set_error(KVC_ERR_UNSUPPORTED,
                      "B*H_kv*G*W too large for the allocation-free pass 1: needs %lld bytes of scratch, "
                      "the fixed array holds %zu",
-                     (long long)(per_range * (int64_t)sizeof(float)), kNoAllocScratchBytes);
-  int np = parts_per_head((int)BH);
-  if (np <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
-  np = (int)std::min<int64_t>(np, (int64_t)kNoAllocScratchFloats / per_range);
-  np = std::max(np, 1);
+                     (long long)((int64_t)BH * per_slot * (int64_t)sizeof(float)), kNoAllocScratchBytes);
+  if (num_sms() <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  ScanPlan pl = make_plan(BH, S);
+  if ((int64_t)pl.P * pl.maxseg * per_slot > (int64_t)kNoAllocScratchFloats) pl = plan_for(BH, S, BH);
+  const int64_t slots = (int64_t)pl.P * pl.maxseg;
 
   float* scratch = nullptr;
   int rc = scratch_on_current_device(&scratch);
   if (rc != KVC_OK) return rc;
   float* pm = scratch;
-  float* pz = scratch + BH * np * gwp;
+  float* pz = scratch + slots * gwp;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
   auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
-  cudaError_t e = launch_pass1(q, kk, B, H_q, H_kv, S, D, W, np, gwp, pm, pz, st);
+  cudaError_t e = launch_pass1(q, kk, B, H_q, H_kv, S, D, W, pl, gwp, pm, pz, st);
   if (e != cudaSuccess) return cuda_error(e, "allocation-free pass 1 launch");
-  e = launch_pass1_combine(pm, pz, B, H_q, H_kv, W, D, np, gwp, S, m, Z, st);
+  e = launch_pass1_combine(pm, pz, B, H_q, H_kv, S, W, pl, gwp, m, Z, st);
   if (e != cudaSuccess) return cuda_error(e, "allocation-free pass 1 combine launch");
   return KVC_OK;
 }

@@ -24,15 +24,26 @@ constexpr int kSelThreads = 256;
 struct SegView {
   int mode;
   const float* scores;     // mode 0: [BH][S]
-  const uint64_t* cand;    // mode 1: [BH][nparts][cap]
-  const int* cand_cnt;     // mode 1: [BH][nparts]
+  const uint64_t* cand;    // mode 1: [slots][cap]
+  const int* cand_cnt;     // mode 1: [slots]
   int cap;
 };
 
-// Number of entries and (score bits, index) of entry i of range `part` of
-// segment `seg`.
+// Candidate slot of range `part` of head `seg` (mode 1), or -1 past the last
+// scan CTA that touches the head.
+__device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int part) {
+  const int64_t S = sp.S;
+  const int64_t c_first = ((int64_t)seg * S) / sp.L;
+  const int64_t c_last = (((int64_t)seg + 1) * S - 1) / sp.L;
+  const int64_t c = c_first + part;
+  if (c > c_last) return -1;
+  return c * sp.maxseg + (seg - (c * sp.L) / S);
+}
+
+// Number of entries of range `part` of head `seg`; for mode 0 also the first
+// key index of the range, for mode 1 the slot.
 __device__ __forceinline__ int range_len(const SegView& v, const SelParams& sp, int seg, int part,
-                                         int* first) {
+                                         int64_t* first) {
   if (v.mode == 0) {
     const int ncand = sp.r_hi - sp.r_lo;
     const int per = (ncand + sp.nparts - 1) / sp.nparts;
@@ -41,18 +52,20 @@ __device__ __forceinline__ int range_len(const SegView& v, const SelParams& sp, 
     *first = sp.r_lo + lo;
     return max(0, hi - lo);
   }
-  *first = 0;
-  return v.cand_cnt[(size_t)seg * sp.nparts + part];
+  const int64_t slot = cand_slot(sp, seg, part);
+  *first = slot;
+  return slot < 0 ? 0 : min(max(v.cand_cnt[slot], 0), v.cap);
 }
 
 __device__ __forceinline__ void entry_at(const SegView& v, const SelParams& sp, int seg, int part,
-                                         int first, int i, uint32_t* u, int* j) {
+                                         int64_t first, int i, uint32_t* u, int* j) {
+  (void)part;
   if (v.mode == 0) {
-    *j = first + i;
+    *j = (int)first + i;
     uint32_t bits = __float_as_uint(v.scores[(size_t)seg * sp.S + first + i]);
     *u = (bits == 0x80000000u) ? 0u : bits;
   } else {
-    const uint64_t e = v.cand[((size_t)seg * sp.nparts + part) * v.cap + i];
+    const uint64_t e = v.cand[(size_t)first * v.cap + i];
     *u = (uint32_t)(e >> 32);
     *j = (int)(uint32_t)e;
   }
@@ -61,7 +74,11 @@ __device__ __forceinline__ void entry_at(const SegView& v, const SelParams& sp, 
 __device__ __forceinline__ int seg_total(const SegView& v, const SelParams& sp, int seg) {
   if (v.mode == 0) return sp.r_hi - sp.r_lo;
   int t = 0;
-  for (int p = 0; p < sp.nparts; ++p) t += v.cand_cnt[(size_t)seg * sp.nparts + p];
+  for (int p = 0; p < sp.nparts; ++p) {
+    const int64_t slot = cand_slot(sp, seg, p);
+    if (slot < 0) break;
+    t += min(max(v.cand_cnt[slot], 0), v.cap);
+  }
   return t;
 }
 
@@ -130,7 +147,7 @@ kvc_hist_kernel(SegView v, const __grid_constant__ SelParams sp, int round, uint
   const int nb = round == 2 ? kHist3 : kHist1;
   for (int i = threadIdx.x; i < nb; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  int first;
+  int64_t first;
   const int len = range_len(v, sp, seg, part, &first);
   for (int i = threadIdx.x; i < len; i += blockDim.x) {
     uint32_t u;
@@ -173,7 +190,7 @@ kvc_count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t
   uint32_t T;
   int need_eq, mode;
   threshold(v, sp, seg, hist, &fs, &T, &need_eq, &mode);
-  int first;
+  int64_t first;
   const int len = range_len(v, sp, seg, part, &first);
   int gt = 0, eq = 0;
   if (mode == 1) {
@@ -231,7 +248,7 @@ kvc_write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t
   out_before = fs.digit;
   eq_before = fs.need;
   __syncthreads();
-  int first;
+  int64_t first;
   const int len = range_len(v, sp, seg, part, &first);
   int written = 0, eq_seen = 0;
   for (int base = 0; base < len; base += blockDim.x) {
@@ -323,9 +340,7 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
 
 cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* idx, int B,
                           int H_kv, int S, int D, int64_t T, const int64_t* off_host,
-                          const int* kept_host, __nv_bfloat16* k_out, __nv_bfloat16* v_out,
-                          int32_t* pos_out, cudaStream_t st) {
-  (void)kept_host;
+                          __nv_bfloat16* k_out, __nv_bfloat16* v_out, int32_t* pos_out, cudaStream_t st) {
   SelParams sp{};
   sp.S = S;
   sp.H_kv = H_kv;

@@ -24,7 +24,7 @@ KVC_ERR_WORKSPACE = -3
 KVC_ERR_CUDA = -4
 KVC_ERR_TIMEOUT = -5
 KVC_ERR_DEVICE = -6
-KVC_OPT_PARTS_PER_HEAD = 1
+KVC_OPT_SCAN_CTAS = 1
 
 _NAMES = {
     KVC_ERR_INVALID_ARG: "invalid argument", KVC_ERR_UNSUPPORTED: "unsupported",

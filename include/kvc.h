@@ -195,7 +195,7 @@ int kvc_check_status(kvc_stream_t stream);
 
 /* Tuning knobs (process-wide, not thread-safe; 0 restores the default). */
 enum kvc_option {
-  KVC_OPT_PARTS_PER_HEAD = 1  /* key ranges per (b, KV head); default from the SM count */
+  KVC_OPT_SCAN_CTAS = 1  /* CTAs (key ranges) of the two scans; default: the SM count */
 };
 int kvc_set_option(int option, int64_t value);
 

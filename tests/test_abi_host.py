@@ -53,7 +53,7 @@ def test_workspace_size_has_no_S_argument():
 
 
 def test_version(K):
-    assert K.kvc_version() == 100
+    assert K.kvc_version() == 200
 
 
 def _call_compress(K, **over):

@@ -83,22 +83,23 @@ def test_small_compress_layer_every_head(K, name):
                                  f"{name} compress b={b} h={h}")
 
 
-@pytest.mark.parametrize("parts", [1, 2, 3])
-def test_candidate_compaction_path(K, parts):
-    """Few key ranges per head: each range sees far more keys than its
-    candidate capacity (K_l_max + b_s), so the in-kernel compaction runs."""
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5])
+def test_candidate_compaction_path(K, ctas):
+    """Few scan CTAs: each key range sees far more keys than its candidate
+    capacity (K_l_max + b_s), so the in-kernel compaction runs; with an odd
+    CTA count the ranges also straddle the two heads."""
     cfg = get_config("tiny", S=6000, C=6000, H_q=8, H_kv=2, D=128, W=32, pool_k=7, K_l=200, recent=32,
-                     b_s=128, hh_frac=0.02, seed=30 + parts)
+                     b_s=128, hh_frac=0.02, seed=30 + ctas)
     inp = make_layer_inputs(cfg)
     K_l, K_l_ref = U.kl_vector(cfg, K)
-    K.kvc_set_option(K.KVC_OPT_PARTS_PER_HEAD, parts)
+    K.kvc_set_option(K.KVC_OPT_SCAN_CTAS, ctas)
     try:
         k_out, v_out, pos, off = U.run_compress(K, cfg, inp, K_l)
     finally:
-        K.kvc_set_option(K.KVC_OPT_PARTS_PER_HEAD, 0)
+        K.kvc_set_option(K.KVC_OPT_SCAN_CTAS, 0)
     for h in range(cfg.H_kv):
         o = U.oracle_head(cfg, inp, 0, h)
-        U.check_head_outputs(k_out, v_out, pos, off, inp, cfg, 0, h, K_l_ref[h], o["s"], f"compaction parts={parts} h={h}")
+        U.check_head_outputs(k_out, v_out, pos, off, inp, cfg, 0, h, K_l_ref[h], o["s"], f"compaction ctas={ctas} h={h}")
 
 
 def _select_case(K, S, H_kv, B, K_l, sink, recent, scores64):
