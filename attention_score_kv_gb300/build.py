@@ -38,9 +38,16 @@ def _run(cmd):
     return p.returncode, " ".join(cmd), p.stdout
 
 
-def build(verbose: bool = False, extra_flags=None, force: bool = False) -> str:
-    """Compile csrc/*.cu for sm_103a and link libkvc.so; returns its path."""
+def build(verbose: bool = False, extra_flags=None, force: bool = False, lib_path: str | None = None,
+          build_dir: str | None = None) -> str:
+    """Compile csrc/*.cu for sm_103a and link libkvc.so; returns its path.
+
+    ``extra_flags`` are appended to every nvcc compile; ``lib_path`` and
+    ``build_dir`` place the library and objects elsewhere (default: in-tree).
+    """
     nvcc = _nvcc()
+    LIB = lib_path or globals()["LIB"]
+    BUILD = build_dir or globals()["BUILD"]
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]

@@ -143,6 +143,7 @@ bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int
   L->gwp = (gw + 15) / 16 * 16;
   L->cap = std::max(K_l_max, 0) + b_s;
   size_t o = 0;
+  L->off_bias = o;     o = align256(o + (size_t)BH * L->gwp * sizeof(float));
   L->off_part_m = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
   L->off_part_z = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
   L->off_hist = o;     o = align256(o + (size_t)BH * kHistPerSeg * sizeof(uint32_t));
@@ -294,23 +295,23 @@ int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, in
 int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* m, const float* Z, int B, int H_q,
                          int H_kv, int S, int D, int W, int b_s, int pool_k, float* scores, void* ws,
                          size_t ws_bytes, kvc_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   int rc;
   if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s)) || (rc = check_pool(pool_k))) return rc;
   if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(m, 4, "m")) ||
       (rc = check_ptr(Z, 4, "Z")) || (rc = check_ptr(scores, 4, "scores")))
     return rc;
-  if (num_sms() <= 0) return set_error(KVC_ERR_CUDA, "no CUDA device");
-  const ScanPlan pl = make_plan(B * H_kv, S);
-  const int gwp = ((H_q / H_kv) * W + 15) / 16 * 16;
+  WsLayout L;
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, 0, pool_k, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  if ((rc = check_ws(ws, ws_bytes, L.off_bias + (size_t)B * H_kv * L.gwp * sizeof(float)))) return rc;
   SelParams sp{};
   sp.S = S;
   sp.H_kv = H_kv;
   Pass2Out out{scores, nullptr, nullptr, 0};
+  float* bias = reinterpret_cast<float*>(static_cast<char*>(ws) + L.off_bias);
   return launch_status(launch_pass2(reinterpret_cast<const __nv_bfloat16*>(q_win),
-                                    reinterpret_cast<const __nv_bfloat16*>(k), m, Z, nullptr, nullptr, B, H_q, H_kv,
-                                    S, D, W, pool_k, pl, gwp, &sp, out, reinterpret_cast<cudaStream_t>(stream)),
+                                    reinterpret_cast<const __nv_bfloat16*>(k), m, Z, nullptr, nullptr, bias, B, H_q,
+                                    H_kv, S, D, W, pool_k, L.plan, L.gwp, &sp, out,
+                                    reinterpret_cast<cudaStream_t>(stream)),
                        "pass 2 launch");
 }
 
@@ -393,9 +394,10 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
     return rc;
   if (ev) cudaEventRecord(ev[1], st);
   Pass2Out out{nullptr, cand, cnt, L.cap};
-  if ((rc = launch_status(
-           launch_pass2(q, kk, nullptr, nullptr, pm, pz, B, H_q, H_kv, S, D, W, pool_k, L.plan, L.gwp, &sp, out, st),
-           "pass 2 launch")))
+  float* bias = reinterpret_cast<float*>(w + L.off_bias);
+  if ((rc = launch_status(launch_pass2(q, kk, nullptr, nullptr, pm, pz, bias, B, H_q, H_kv, S, D, W, pool_k, L.plan,
+                                       L.gwp, &sp, out, st),
+                          "pass 2 launch")))
     return rc;
   if (ev) cudaEventRecord(ev[2], st);
   if ((rc = launch_status(launch_select(1, nullptr, cand, cnt, L.cap, B, sp, reinterpret_cast<uint32_t*>(w + L.off_hist),

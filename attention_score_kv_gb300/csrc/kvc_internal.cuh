@@ -44,6 +44,7 @@ struct WsLayout {
   int slots;       // partial / candidate slots reserved
   int gwp;         // G*W rounded up to 16
   int cap;         // candidate capacity per slot (K_l_max + b_s)
+  size_t off_bias;                 // float  [BH][gwp]    pass-2 per-row bias
   size_t off_part_m, off_part_z;   // float  [slots][gwp]
   size_t off_hist;                 // uint32 [BH][kHistPerSeg]
   size_t off_pcnt;                 // int2   [BH][plan.nparts]
@@ -91,8 +92,8 @@ struct Pass2Out {
   int cap;
 };
 cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const float* m, const float* Z,
-                         const float* part_m, const float* part_z, int B, int H_q, int H_kv, int S, int D, int W,
-                         int pool_k, const ScanPlan& pl, int gwp, const SelParams* sel, Pass2Out out,
+                         const float* part_m, const float* part_z, float* bias_ws, int B, int H_q, int H_kv, int S,
+                         int D, int W, int pool_k, const ScanPlan& pl, int gwp, const SelParams* sel, Pass2Out out,
                          cudaStream_t st);
 // selection over dense scores (mode 0) or candidate lists (mode 1)
 cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt, int cap, int B,

@@ -1,0 +1,288 @@
+// Pass 1 of the two-pass scorer (TideKV, Fig. 3): per window query, the
+// log-sum-exp normalisers over the prefix keys, kept as W-length state.
+//
+// A = window queries (two 128-row MMA blocks when G*W > 128), B = 128-key
+// tile.  Eight softmax warps read the accumulators from tensor memory: with
+// two blocks each thread owns one query row and all 128 key columns of a
+// tile; with one block the two warps of a lane quarter split the columns.
+// Each thread keeps a running max (raw dot product units) and the sum of
+// 2^(x - max), x = q.k * log2(e)/sqrt(D), over its segment, then writes the
+// (max * log2(e)/sqrt(D), Z) partial of its row to the segment's slot.
+#include "kvc_scan_common.cuh"
+
+namespace kvc {
+namespace {
+
+using namespace scan;
+
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiThreads) : "memory"); }
+
+// Accumulators rotate through four 128-column tensor-memory buffers, one per
+// (tile, 128-row query block) "sub-tile" u: buffer u & 3, completed once per
+// use, so the (u >> 2)-th use of a buffer waits on parity (u >> 2) & 1.  The
+// MMA warp can run two tiles ahead of the softmax warps.
+template <int D>
+__device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, const Seg* segs, int nseg, uint32_t sQ, uint32_t sK,
+                          uint32_t tmem, volatile int* abort_flag) {
+  constexpr int NKH = D / 64;
+  constexpr int KSTEPS = D / 16;
+  constexpr uint32_t kTileBytes = kTile * 128 * NKH;
+  const uint32_t q_half = (uint32_t)A.nq * 128;
+  const uint32_t idesc = tc::idesc_bf16(128, 128);
+  uint32_t stage = 0, phase = 0, qphase = 0, u = 0;
+  for (int s = 0; s < nseg; ++s) {
+    const Seg sg = segs[s];
+    if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) return;
+    qphase ^= 1;
+    const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status)) return;
+      const uint32_t kb = sK + stage * kTileBytes;
+      for (int mb = 0; mb < A.n_mb; ++mb, ++u) {
+        const uint32_t b = u & 3;
+        if (!wait_bar(smem_u32(&bars->tempty[b]), ((u >> 2) & 1) ^ 1, abort_flag, A.status)) return;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
+          const uint32_t qoff = (ks >> 2) * q_half + mb * (128 * 128) + (ks & 3) * 32;
+          tc::mma_bf16(tmem + b * 128, tc::desc_sw128(sQ + qoff), tc::desc_sw128(kb + koff), idesc, ks > 0);
+        }
+        tc::mma_commit(smem_u32(&bars->tfull[b]));
+      }
+      tc::mma_commit(smem_u32(&bars->empty[stage]));
+      if (++stage == kStages) { stage = 0; phase ^= 1; }
+    }
+    tc::mma_commit(smem_u32(&bars->qempty));
+  }
+}
+
+template <int D, int NMB>
+__global__ void __launch_bounds__(kThreads, 1)
+kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ CUtensorMap qmap,
+                    const __grid_constant__ CUtensorMap kmap) {
+  constexpr int NKH = D / 64;
+  constexpr int NC = NMB == 2 ? 128 : 64;       // accumulator columns per softmax thread
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ PipeBars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ float2 s_half[128];
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = base;
+  const uint32_t sK = base + (uint32_t)A.nq * 128 * NKH;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    init_pipe_bars(&bars, NMB == 2 ? kEpiWarps / 2 : kEpiWarps);
+    s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&qmap);
+      tc::tma_prefetch_desc(&kmap);
+      producer<D, 1>(A, &qmap, &kmap, &bars, sQ, sK, &s_abort);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      Seg segs[kMaxSegs];
+      const int nseg = cta_segments(A, blockIdx.x, segs);
+      mma_pass1<D>(A, &bars, segs, nseg, sQ, sK, tmem, &s_abort);
+    }
+  } else {
+    const int e = warp - 2;
+    const int quarter = warp & 3;              // TMEM lanes this warp may read
+    const int k = e >> 2;                      // 0 or 1
+    const int mb = NMB == 2 ? k : 0;
+    const int col0 = NMB == 2 ? 0 : 64 * k;
+    const int row = mb * 128 + quarter * 32 + lane;
+    const bool active = (mb * 128 + quarter * 32) < A.gw;
+    const float c2 = A.c2;
+    const int t_row = A.S - A.W + (row % A.W);
+    Seg segs[kMaxSegs];
+    const int nseg = cta_segments(A, blockIdx.x, segs);
+    uint32_t tcount = 0;
+    bool ok = true;
+    for (int s = 0; s < nseg && ok; ++s) {
+      const Seg sg = segs[s];
+      float mrun = -INFINITY;
+      float2 z2 = make_float2(0.f, 0.f);
+      const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
+      for (int t = 0; t < ntiles; ++t, ++tcount) {
+        const uint32_t u = NMB == 2 ? 2 * tcount + mb : tcount;   // this warp's sub-tile
+        const uint32_t buf = u & 3;
+        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), (u >> 2) & 1, &s_abort, A.status)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t taddr = tmem + buf * 128 + col0 + ((uint32_t)(quarter * 32) << 16);
+        // 64 accumulator columns at a time; the buffer is handed back to the
+        // MMA warp right after the last batch has been read
+#pragma unroll 1
+        for (int bt = 0; bt < NC / 64; ++bt) {
+          float v[64];
+          if (active) {
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) tc::tmem_ld16(taddr + bt * 64 + c, v + c);
+            tc::tmem_wait_ld();
+            tc::reg_fence(v, 64);
+          }
+          if (bt == NC / 64 - 1) {
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[buf]));
+          }
+          if (!active) continue;
+          const int t0 = sg.a + t * kTile + col0 + bt * 64;
+          if (t0 + 63 >= sg.b || t0 + 63 > A.S - A.W) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const int j = t0 + c;
+              if (j >= sg.b || j > t_row) v[c] = -INFINITY;
+            }
+          }
+          float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+#pragma unroll
+          for (int c = 4; c < 64; c += 4) {
+            mx0 = fmaxf(mx0, fmaxf(v[c], v[c + 1]));
+            mx1 = fmaxf(mx1, fmaxf(v[c + 2], v[c + 3]));
+          }
+          const float mx = fmaxf(mx0, mx1);
+          if (mx > mrun) {
+            const float sc = (mrun == -INFINITY) ? 0.f : ex2((mrun - mx) * c2);
+            z2.x *= sc;
+            z2.y *= sc;
+            mrun = mx;
+          }
+          if (mrun > -INFINITY) {
+            const float nm = -mrun * c2;
+#if KVC_EXP_SCALAR
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f, s6 = 0.f, s7 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+              s0 += ex2(fmaf(v[c], c2, nm));
+              s1 += ex2(fmaf(v[c + 1], c2, nm));
+              s2 += ex2(fmaf(v[c + 2], c2, nm));
+              s3 += ex2(fmaf(v[c + 3], c2, nm));
+              s4 += ex2(fmaf(v[c + 4], c2, nm));
+              s5 += ex2(fmaf(v[c + 5], c2, nm));
+              s6 += ex2(fmaf(v[c + 6], c2, nm));
+              s7 += ex2(fmaf(v[c + 7], c2, nm));
+            }
+            z2.x += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+#else
+            const float2 cc = make_float2(c2, c2), nn = make_float2(nm, nm);
+            float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+              const float2 x0 = __ffma2_rn(make_float2(v[c], v[c + 1]), cc, nn);
+              const float2 x1 = __ffma2_rn(make_float2(v[c + 2], v[c + 3]), cc, nn);
+              const float2 x2 = __ffma2_rn(make_float2(v[c + 4], v[c + 5]), cc, nn);
+              const float2 x3 = __ffma2_rn(make_float2(v[c + 6], v[c + 7]), cc, nn);
+              a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
+              a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
+              a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
+              a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+            }
+            z2 = __fadd2_rn(z2, __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3)));
+#endif
+          }
+        }
+      }
+      if (!ok) break;
+      // segment done: the two column halves of a row (one block) are merged
+      const float2 mine = make_float2(mrun == -INFINITY ? -INFINITY : mrun * c2, z2.x + z2.y);
+      const size_t slot = (size_t)blockIdx.x * A.maxseg + (size_t)(sg.bh - segs[0].bh);
+      if (NMB == 2) {
+        if (row < A.gwp16) {
+          A.part_m[slot * A.gwp16 + row] = mine.x;
+          A.part_z[slot * A.gwp16 + row] = mine.y;
+        }
+      } else {
+        if (k == 1) s_half[quarter * 32 + lane] = mine;
+        epi_sync();
+        if (k == 0 && row < A.gwp16) {
+          const float2 st = merge_mz(mine, s_half[quarter * 32 + lane]);
+          A.part_m[slot * A.gwp16 + row] = st.x;
+          A.part_z[slot * A.gwp16 + row] = st.y;
+        }
+        epi_sync();
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// m, Z (natural-log units) of every window row from the pass-1 slots.
+__global__ void kvc_pass1_combine_kernel(const __grid_constant__ ScanArgs A, float* __restrict__ m,
+                                         float* __restrict__ Z) {
+  const int bh = blockIdx.x;
+  const int b = bh / A.H_kv, h = bh % A.H_kv, G = A.H_q / A.H_kv;
+  for (int r = threadIdx.x; r < A.gw; r += blockDim.x) {
+    const float2 st = combine_partials(A, bh, r);
+    const size_t dst = (size_t)(b * A.H_q + h * G) * A.W + r;
+    m[dst] = st.x / kLog2e;
+    Z[dst] = st.y;
+  }
+}
+
+template <typename Kern>
+cudaError_t launch(Kern kernel, int grid, size_t smem, cudaStream_t st, const ScanArgs& A, const CUtensorMap& qm,
+                   const CUtensorMap& km) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(A, qm, km);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pass1(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S, int D,
+                         int W, const ScanPlan& pl, int gwp, float* part_m, float* part_z, cudaStream_t st) {
+  (void)gwp;
+  ScanArgs A = base_args(pl, B, H_q, H_kv, S, D, W);
+  A.nq = 128 * A.n_mb;
+  A.part_m = part_m;
+  A.part_z = part_z;
+  CUtensorMap qm, km;
+  if (!make_map(&qm, q, D, (uint64_t)B * H_q * W, 1, A.nq) || !make_map(&km, k, D, S, (uint64_t)B * H_kv, kTile))
+    return cudaErrorInvalidValue;
+  const size_t smem = pipe_smem(D, A.nq);
+  if (D == 64)
+    return A.n_mb == 2 ? launch(kvc_tc_pass1_kernel<64, 2>, pl.P, smem, st, A, qm, km)
+                       : launch(kvc_tc_pass1_kernel<64, 1>, pl.P, smem, st, A, qm, km);
+  return A.n_mb == 2 ? launch(kvc_tc_pass1_kernel<128, 2>, pl.P, smem, st, A, qm, km)
+                     : launch(kvc_tc_pass1_kernel<128, 1>, pl.P, smem, st, A, qm, km);
+}
+
+cudaError_t launch_pass1_combine(const float* part_m, const float* part_z, int B, int H_q, int H_kv, int S, int W,
+                                 const ScanPlan& pl, int gwp, float* m, float* Z, cudaStream_t st) {
+  (void)gwp;
+  ScanArgs A = base_args(pl, B, H_q, H_kv, S, 64, W);
+  A.pm_in = part_m;
+  A.pz_in = part_z;
+  kvc_pass1_combine_kernel<<<B * H_kv, 256, 0, st>>>(A, m, Z);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

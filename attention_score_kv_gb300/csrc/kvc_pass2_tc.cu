@@ -1,0 +1,609 @@
+// Pass 2 of the two-pass scorer plus pooling (TideKV, Fig. 3): per key, the
+// normalised attention weights summed over the window queries and the GQA
+// group, average-pooled, then written as scores or appended to the key
+// range's candidate list.
+//
+// A = 128-key tile (M = 128), B = window queries (N = G*W rounded to 16), so
+// tensor-memory lane i holds key i of the tile and the query axis runs along
+// the columns.  The per-query normaliser enters the MMA itself: one extra
+// K-step multiplies a constant (1, 1, 1, 0, ...) block on the key side with
+// the query's bias -lse2_q / (log2(e)/sqrt(D)), split into three bf16 terms
+// (hi, mid, lo) on the query side, so the accumulator already holds
+// q.k - lse_q in raw units and a weight is 2^(acc * log2(e)/sqrt(D)).
+//
+// Two groups of four softmax warps take alternate tiles (group g reads
+// accumulator buffer g); each thread owns one key and sums its weights over
+// every column in registers, then hands the key's mass r_j to a shared-memory
+// ring.  A pooling warp consumes the ring in key order: it keeps the last
+// pool_k-1 masses of the previous tile, forms the centred average for keys
+// t0 - h .. t0 + 127 - h, and appends the non-mandatory keys that beat the
+// range's running threshold.
+#include "kvc_scan_common.cuh"
+
+namespace kvc {
+namespace {
+
+using namespace scan;
+
+constexpr int kStages2 = 3;
+constexpr int kGroupWarps = 4;                   // one warp per TMEM lane quarter
+constexpr int kPoolWarp = 2 + 2 * kGroupWarps;   // warp 10
+constexpr int kThreads = 32 * (kPoolWarp + 1);
+constexpr int kRing = 4;
+constexpr int kRingPad = 16;                     // room for the previous tile's last 2h masses
+constexpr float kNoWeight = -1.0e30f;            // bias of padding rows: weight 0
+
+struct RingBars {
+  uint64_t rfull[kRing], rempty[kRing], bias_free;
+};
+
+struct WarpCompact {
+  int hist[256];
+};
+
+__device__ __forceinline__ uint64_t rank_key(uint64_t e) {
+  // (score bits, ~index): larger is better, the lower index wins a score tie
+  return (e & 0xFFFFFFFF00000000ull) | (uint64_t)(~(uint32_t)e);
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// One warp keeps the n_keep best entries of buf[0..cnt) in place (order
+// kept) by an 8-bit radix select on rank_key, and returns the new count;
+// *tau becomes the score bits a later (higher-index) key must beat.
+__device__ int warp_compact(uint64_t* buf, int cnt, int n_keep, WarpCompact* wc, long long* tau, int* status) {
+  const int lane = threadIdx.x & 31;
+  if (n_keep <= 0) {
+    *tau = LLONG_MAX;
+    return 0;
+  }
+  unsigned long long prefix = 0;
+  int need = n_keep;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = lane; i < 256; i += 32) wc->hist[i] = 0;
+    __syncwarp();
+    for (int i = lane; i < cnt; i += 32) {
+      const uint64_t key = rank_key(buf[i]);
+      if (shift == 56 || (key >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&wc->hist[(key >> shift) & 255], 1);
+    }
+    __syncwarp();
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) local += wc->hist[255 - 8 * lane - i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int before = incl - local;
+    int d = -1, nd = 0, full = 0;
+    if (before < need && need <= incl) {
+      int cum = before;
+      for (int i = 0; i < 8; ++i) {
+        const int c = wc->hist[255 - 8 * lane - i];
+        if (cum + c >= need) {
+          d = 255 - 8 * lane - i;
+          nd = need - cum;
+          full = (nd == c);
+          break;
+        }
+        cum += c;
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, d >= 0);
+    __syncwarp();
+    if (bal == 0) {  // inconsistent counts: keep everything
+      if (lane == 0) record_status(status, kStatusCandOverflow);
+      *tau = -1;
+      return cnt;
+    }
+    const int src = __ffs(bal) - 1;
+    d = __shfl_sync(0xffffffffu, d, src);
+    nd = __shfl_sync(0xffffffffu, nd, src);
+    full = __shfl_sync(0xffffffffu, full, src);
+    prefix |= (unsigned long long)d << shift;
+    need = nd;
+    if (full) break;
+  }
+  const uint64_t T = prefix;
+  int out = 0;
+  for (int b0 = 0; b0 < cnt; b0 += 32) {
+    const int i = b0 + lane;
+    const uint64_t e = i < cnt ? buf[i] : 0ull;
+    const bool f = i < cnt && rank_key(e) >= T;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    __syncwarp();
+    if (f) buf[out + __popc(bal & ((1u << lane) - 1u))] = e;
+    out += __popc(bal);
+    __syncwarp();
+  }
+  if (out != n_keep && lane == 0) record_status(status, kStatusCandOverflow);
+  *tau = (long long)(T >> 32);
+  return out;
+}
+
+// Whole warp: writes the bias operand of each segment (after the previous
+// segment's MMAs are done with it); lane 0 issues the MMAs.
+template <int D>
+__device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const Seg* segs, int nseg, uint32_t sQ,
+                         uint32_t sK, uint32_t sOnes, uint32_t sBias, uint32_t tmem, volatile int* abort_flag) {
+  constexpr int NKH = D / 64;
+  constexpr int KSTEPS = D / 16;
+  constexpr uint32_t kTileBytes = kTile * 128 * NKH;
+  const int lane = threadIdx.x & 31;
+  const uint32_t q_half = (uint32_t)A.nq * 128;
+  const int hw = (A.pool_k - 1) / 2;
+  const uint32_t idesc = tc::idesc_bf16(128, A.gwp16);
+  // key side of the bias K-step: row r, K elements 0..2 = 1.0, the rest 0
+  // (128-byte swizzle: logical 16-byte chunk c of row r sits at chunk c ^ (r & 7))
+  for (int idx = lane; idx < kTile * 8; idx += 32) {
+    const int row = idx >> 3, pch = idx & 7;
+    const bool first = (pch ^ (row & 7)) == 0;
+    const uint4 val = first ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(sOnes + idx * 16), "r"(val.x), "r"(val.y),
+                 "r"(val.z), "r"(val.w)
+                 : "memory");
+  }
+  // query side: only logical chunk 0 of each row ever holds data
+  for (int idx = lane; idx < A.nq * 8; idx += 32)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(sBias + idx * 16), "r"(0u) : "memory");
+  uint32_t stage = 0, phase = 0, qphase = 0, buf = 0, tphase = 0, bphase = 0;
+  for (int s = 0; s < nseg; ++s) {
+    const Seg sg = segs[s];
+    int okl = 1;
+    if (s > 0) {
+      if (lane == 0) okl = wait_bar(smem_u32(&rb->bias_free), bphase, abort_flag, A.status);
+      bphase ^= 1;
+    }
+    if (!__shfl_sync(0xffffffffu, okl, 0)) return;
+    // query side: row q, K elements 0..2 = bias split into three bf16 terms;
+    // lane l handles rows l, l+32, ...: all loads first, then the stores
+    float bv[kMaxGWP / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxGWP / 32; ++i) {
+      const int row = lane + 32 * i;
+      bv[i] = (row < A.gwp16) ? A.bias[(size_t)sg.bh * A.gwp16 + row] : kNoWeight;
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxGWP / 32; ++i) {
+      const int row = lane + 32 * i;
+      if (row < A.nq) {
+        const float b = bv[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(b);
+        const float r1 = b - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        const uint32_t x = bf16_bits(__bfloat162float(hi)) | (bf16_bits(__bfloat162float(mid)) << 16);
+        const uint32_t y = bf16_bits(r2);
+        // logical chunk 0 of row `row` sits at physical chunk (row & 7)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %3};\n" ::"r"(sBias + row * 128 + (row & 7) * 16), "r"(x),
+                     "r"(y), "r"(0u)
+                     : "memory");
+      }
+    }
+    tc::fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) okl = 0;
+      qphase ^= 1;
+      const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
+      for (int t = 0; t < ntiles && okl; ++t) {
+        if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status) ||
+            !wait_bar(smem_u32(&bars->tempty[buf]), tphase ^ 1, abort_flag, A.status)) {
+          okl = 0;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t kb = sK + stage * kTileBytes;
+        const uint32_t dacc = tmem + buf * kAccStride;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
+          const uint32_t qoff = (ks >> 2) * q_half + (ks & 3) * 32;
+          tc::mma_bf16(dacc, tc::desc_sw128(kb + koff), tc::desc_sw128(sQ + qoff), idesc, ks > 0);
+        }
+        tc::mma_bf16(dacc, tc::desc_sw128(sOnes), tc::desc_sw128(sBias), idesc, 1);
+        tc::mma_commit(smem_u32(&bars->empty[stage]));
+        tc::mma_commit(smem_u32(&bars->tfull[buf]));
+        if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        if (++buf == 2) { buf = 0; tphase ^= 1; }
+      }
+      if (okl) {
+        tc::mma_commit(smem_u32(&bars->qempty));
+        tc::mma_commit(smem_u32(&rb->bias_free));
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, okl, 0)) return;
+  }
+}
+
+template <int D, bool CAND>
+__global__ void __launch_bounds__(kThreads, 1)
+kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ SelParams sel,
+                    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap) {
+  constexpr int NKH = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ PipeBars bars;
+  __shared__ RingBars rbars;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ float s_ring[kRing][kRingPad + kTile];
+  __shared__ WarpCompact s_wc;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = base;
+  const uint32_t sK = sQ + (uint32_t)A.nq * 128 * NKH;
+  const uint32_t sOnes = sK + kStages2 * kTile * 128 * NKH;
+  const uint32_t sBias = sOnes + kTile * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    init_pipe_bars(&bars, kGroupWarps, kStages2);
+    for (int i = 0; i < kRing; ++i) {
+      tc::mbar_init(smem_u32(&rbars.rfull[i]), kGroupWarps * 32);
+      tc::mbar_init(smem_u32(&rbars.rempty[i]), 1);
+    }
+    tc::mbar_init(smem_u32(&rbars.bias_free), 1);
+    s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  const int hw = (A.pool_k - 1) / 2;
+  Seg segs[kMaxSegs];
+  const int nseg = cta_segments(A, blockIdx.x, segs);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&qmap);
+      tc::tma_prefetch_desc(&kmap);
+      producer<D, 2, kStages2>(A, &qmap, &kmap, &bars, sQ, sK, &s_abort);
+    }
+  } else if (warp == 1) {
+    mma_warp<D>(A, &bars, &rbars, segs, nseg, sQ, sK, sOnes, sBias, tmem, &s_abort);
+  } else if (warp < kPoolWarp) {
+    // ---------------------------------------------------- softmax warps
+    const int g = (warp - 2) / kGroupWarps;
+    const int quarter = warp & 3;
+    const int krow = quarter * 32 + lane;
+    const int nch = A.gwp16 / 16;
+    const int nbt = (nch + 3) / 4;
+    const float c2 = A.c2;
+    const float2 cc = make_float2(c2, c2);
+    const uint32_t taddr = tmem + g * kAccStride + ((uint32_t)(quarter * 32) << 16);
+    uint32_t tph = 0;
+    int tcount = 0;
+    bool ok = true;
+    for (int s = 0; s < nseg && ok; ++s) {
+      const Seg sg = segs[s];
+      const int n_iter = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
+      for (int it = 0; it < n_iter; ++it, ++tcount) {
+        if ((tcount & 1) != g) continue;
+        const int t0 = sg.a - hw + it * kTile;
+        if (!wait_bar_warp(smem_u32(&bars.tfull[g]), tph, &s_abort, A.status)) { ok = false; break; }
+        tph ^= 1;
+        tc::fence_after_sync();
+        const int j = t0 + krow;
+        const bool need_mask = (t0 + kTile - 1 > A.S - A.W);
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#if KVC_TMEM_PIPE
+        // next batch's tensor-memory loads in flight while this batch is summed
+        float va[64], vb[64];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < nch) tc::tmem_ld16(taddr + i * 16, va + 16 * i);
+        tc::tmem_wait_ld();
+        tc::reg_fence(va, 64);
+#pragma unroll
+        for (int bt = 0; bt < 4; ++bt) {
+          if (bt < nbt) {
+            float(&cur)[64] = (bt & 1) ? vb : va;
+            float(&nxt)[64] = (bt & 1) ? va : vb;
+            if (bt + 1 < nbt) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (4 * (bt + 1) + i < nch) tc::tmem_ld16(taddr + (4 * (bt + 1) + i) * 16, nxt + 16 * i);
+            } else {
+              tc::fence_before_sync();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[g]));
+            }
+            if (!need_mask) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (4 * bt + i < nch) {
+#pragma unroll
+                  for (int q = 0; q < 16; q += 8) {
+                    const float* w = cur + 16 * i + q;
+                    a0.x += ex2(w[0] * c2);
+                    a0.y += ex2(w[1] * c2);
+                    a1.x += ex2(w[2] * c2);
+                    a1.y += ex2(w[3] * c2);
+                    a2.x += ex2(w[4] * c2);
+                    a2.y += ex2(w[5] * c2);
+                    a3.x += ex2(w[6] * c2);
+                    a3.y += ex2(w[7] * c2);
+                  }
+                }
+              }
+            } else {
+              const int dj = j - (A.S - A.W);
+              for (int i = 0; i < 4; ++i) {
+                if (4 * bt + i < nch) {
+                  int wi = ((4 * bt + i) * 16) % A.W;
+                  for (int q = 0; q < 16; ++q) {
+                    const float e = ex2(cur[16 * i + q] * c2);
+                    a0.x += wi >= dj ? e : 0.f;
+                    if (++wi == A.W) wi = 0;
+                  }
+                }
+              }
+            }
+            if (bt + 1 < nbt) {
+              tc::tmem_wait_ld();
+              tc::reg_fence(nxt, 64);
+            }
+          }
+        }
+#else
+#pragma unroll 1
+        for (int bt = 0; bt < nbt; ++bt) {
+          float v[64];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (4 * bt + i < nch) tc::tmem_ld16(taddr + (4 * bt + i) * 16, v + 16 * i);
+          tc::tmem_wait_ld();
+          tc::reg_fence(v, 64);
+          if (bt == nbt - 1) {
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[g]));
+          }
+          if (!need_mask) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (4 * bt + i < nch) {
+#pragma unroll
+                for (int q = 0; q < 16; q += 8) {
+                  const float* w = v + 16 * i + q;
+#if KVC_EXP_SCALAR
+                  a0.x += ex2(w[0] * c2);
+                  a0.y += ex2(w[1] * c2);
+                  a1.x += ex2(w[2] * c2);
+                  a1.y += ex2(w[3] * c2);
+                  a2.x += ex2(w[4] * c2);
+                  a2.y += ex2(w[5] * c2);
+                  a3.x += ex2(w[6] * c2);
+                  a3.y += ex2(w[7] * c2);
+#else
+                  const float2 x0 = __fmul2_rn(make_float2(w[0], w[1]), cc);
+                  const float2 x1 = __fmul2_rn(make_float2(w[2], w[3]), cc);
+                  const float2 x2 = __fmul2_rn(make_float2(w[4], w[5]), cc);
+                  const float2 x3 = __fmul2_rn(make_float2(w[6], w[7]), cc);
+                  a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
+                  a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
+                  a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
+                  a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+#endif
+                }
+              }
+            }
+          } else {
+            // tiles near the window: window query i (column g*W + i) sees key
+            // j only when j <= S - W + i, i.e. i >= dj
+            const int dj = j - (A.S - A.W);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (4 * bt + i < nch) {
+                int wi = ((4 * bt + i) * 16) % A.W;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                  const float e = ex2(v[16 * i + q] * c2);
+                  a0.x += wi >= dj ? e : 0.f;
+                  if (++wi == A.W) wi = 0;
+                }
+              }
+            }
+          }
+        }
+#endif
+        float r = (a0.x + a0.y) + (a1.x + a1.y) + ((a2.x + a2.y) + (a3.x + a3.y));
+        if (j < 0 || j >= A.S) r = 0.f;
+        const int slot = tcount % kRing;
+        if (!wait_bar_warp(smem_u32(&rbars.rempty[slot]), ((tcount / kRing) & 1) ^ 1, &s_abort, A.status)) {
+          ok = false;
+          break;
+        }
+        s_ring[slot][kRingPad + krow] = r;
+        tc::mbar_arrive(smem_u32(&rbars.rfull[slot]));
+      }
+    }
+  } else {
+    // ------------------------------------------------------- pooling warp
+    const float inv_pool = 1.0f / (float)A.pool_k;
+    int tcount = 0;
+    bool ok = true;
+    for (int s = 0; s < nseg && ok; ++s) {
+      const Seg sg = segs[s];
+      const int hk = sg.bh % A.H_kv;
+      const size_t slot_id = (size_t)blockIdx.x * A.maxseg + (size_t)(sg.bh - segs[0].bh);
+      uint64_t* my_cand = CAND ? A.cand + slot_id * A.cap : nullptr;
+      const int n_keep = CAND ? sel.n_sel[hk] : 0;
+      int cnt = 0;
+      long long tau = -1;
+      const int n_iter = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
+      for (int it = 0; it < n_iter; ++it, ++tcount) {
+        const int t0 = sg.a - hw + it * kTile;
+        const int slot = tcount % kRing;
+        float* rr = s_ring[slot];   // [kRingPad - 2h, kRingPad): previous tile's last masses
+        if (it == 0) {
+          if (lane < kRingPad) rr[lane] = 0.f;   // keys before the segment's first tile: none
+          __syncwarp();
+        }
+        if (!wait_bar_warp(smem_u32(&rbars.rfull[slot]), (tcount / kRing) & 1, &s_abort, A.status)) { ok = false; break; }
+        // lane l pools keys t0 - h + 4l + k, k = 0..3, over masses win[k .. k + 2h]
+        const float* win = rr + kRingPad - 2 * hw + 4 * lane;
+        float sc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float acc = 0.f;
+          for (int d = 0; d <= 2 * hw; ++d) acc += win[k + d];
+          sc[k] = A.pool_k == 1 ? acc : acc * inv_pool;
+        }
+        const int j0 = t0 - hw + 4 * lane;
+        if (!CAND) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (j0 + k >= sg.a && j0 + k < sg.b) A.scores[(size_t)sg.bh * A.S + j0 + k] = sc[k];
+        } else {
+          uint32_t u[4];
+          bool is_cand[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            u[k] = __float_as_uint(sc[k]);
+            if (u[k] == 0x80000000u) u[k] = 0u;
+            const int jo = j0 + k;
+            is_cand[k] = jo >= sg.a && jo < sg.b && jo >= sel.r_lo && jo < sel.r_hi;
+          }
+          for (int tries = 0;; ++tries) {
+            int n_mine = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) n_mine += (is_cand[k] && (long long)u[k] > tau) ? 1 : 0;
+            int incl = n_mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int t = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += t;
+            }
+            const int n_new = __shfl_sync(0xffffffffu, incl, 31);
+            if (cnt + n_new > A.cap) {
+              if (cnt <= n_keep || tries >= 2) {
+                if (lane == 0) record_status(A.status, kStatusCandOverflow);
+                break;
+              }
+              cnt = warp_compact(my_cand, cnt, n_keep, &s_wc, &tau, A.status);
+              continue;
+            }
+            int pos = cnt + incl - n_mine;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (is_cand[k] && (long long)u[k] > tau) {
+                my_cand[pos++] = ((uint64_t)u[k] << 32) | (uint32_t)(j0 + k);
+              }
+            }
+            cnt += n_new;
+            break;
+          }
+        }
+        // the next tile of this segment pools over this tile's last 2h masses
+        if (it + 1 < n_iter && lane < 2 * hw)
+          s_ring[(tcount + 1) % kRing][kRingPad - 2 * hw + lane] = rr[kRingPad + kTile - 2 * hw + lane];
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(smem_u32(&rbars.rempty[slot]));
+      }
+      if (CAND && ok && lane == 0) A.cand_cnt[slot_id] = cnt;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Bias of every window row: -lse2 / (log2(e)/sqrt(D)), from (m, Z) in
+// natural units or from the pass-1 slots; padding rows get no weight.
+// One warp per window row: the lanes merge the row's pass-1 slots in
+// parallel, then a butterfly merges the lanes.
+__global__ void kvc_lse_bias_kernel(const __grid_constant__ ScanArgs A, float* __restrict__ bias) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int r = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (r >= A.gwp16) return;
+  const int b = bh / A.H_kv, h = bh % A.H_kv, G = A.H_q / A.H_kv;
+  float out = kNoWeight;
+  if (r < A.gw) {
+    float lse2;
+    if (A.m_in != nullptr) {
+      const size_t src = (size_t)(b * A.H_q + h * G) * A.W + r;
+      lse2 = A.m_in[src] * kLog2e + log2f(A.z_in[src]);
+    } else {
+      const int64_t S = A.S;
+      const int c_first = (int)(((int64_t)bh * S) / A.L);
+      const int c_last = (int)((((int64_t)bh + 1) * S - 1) / A.L);
+      float2 st = make_float2(-INFINITY, 0.f);
+      for (int c = c_first + lane; c <= c_last; c += 32) {
+        const int seg = bh - (int)(((int64_t)c * A.L) / S);
+        const size_t o = ((size_t)c * A.maxseg + seg) * A.gwp16 + r;
+        st = merge_mz(st, make_float2(A.pm_in[o], A.pz_in[o]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, st.x, o), __shfl_xor_sync(0xffffffffu, st.y, o));
+        st = merge_mz(st, other);
+      }
+      lse2 = st.x + log2f(st.y);
+    }
+    out = -lse2 / A.c2;
+  }
+  if (lane == 0) bias[(size_t)bh * A.gwp16 + r] = out;
+}
+
+template <typename Kern>
+cudaError_t launch(Kern kernel, int grid, size_t smem, cudaStream_t st, const ScanArgs& A, const SelParams& sp,
+                   const CUtensorMap& qm, const CUtensorMap& km) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(A, sp, qm, km);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const float* m, const float* Z,
+                         const float* part_m, const float* part_z, float* bias_ws, int B, int H_q, int H_kv, int S,
+                         int D, int W, int pool_k, const ScanPlan& pl, int gwp, const SelParams* sel, Pass2Out out,
+                         cudaStream_t st) {
+  (void)gwp;
+  ScanArgs A = base_args(pl, B, H_q, H_kv, S, D, W);
+  A.nq = A.gwp16;
+  A.pool_k = pool_k;
+  A.m_in = m;
+  A.z_in = Z;
+  A.pm_in = part_m;
+  A.pz_in = part_z;
+  A.bias = bias_ws;
+  A.scores = out.scores;
+  A.cand = out.cand;
+  A.cand_cnt = out.cand_cnt;
+  A.cap = out.cap;
+  kvc_lse_bias_kernel<<<dim3((A.gwp16 + 7) / 8, B * H_kv), 256, 0, st>>>(A, bias_ws);
+  note_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap qm, km;
+  if (!make_map(&qm, q, D, (uint64_t)B * H_q * W, 1, A.nq) || !make_map(&km, k, D, S, (uint64_t)B * H_kv, kTile))
+    return cudaErrorInvalidValue;
+  const size_t smem = 1024 + (size_t)A.nq * 128 * (D / 64) + (size_t)kStages2 * kTile * 128 * (D / 64) +
+                      (size_t)kTile * 128 + (size_t)A.nq * 128;
+  const bool cand = out.cand != nullptr;
+  if (D == 64)
+    return cand ? launch(kvc_tc_pass2_kernel<64, true>, pl.P, smem, st, A, *sel, qm, km)
+                : launch(kvc_tc_pass2_kernel<64, false>, pl.P, smem, st, A, *sel, qm, km);
+  return cand ? launch(kvc_tc_pass2_kernel<128, true>, pl.P, smem, st, A, *sel, qm, km)
+              : launch(kvc_tc_pass2_kernel<128, false>, pl.P, smem, st, A, *sel, qm, km);
+}
+
+}  // namespace kvc

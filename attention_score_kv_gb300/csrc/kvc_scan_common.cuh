@@ -1,0 +1,291 @@
+// Pieces shared by the two scans of the two-pass scorer (TideKV, Fig. 3):
+// the work split, the TMA producer, the tcgen05 MMA issuer and host-side
+// tensor-map set-up.
+//
+// Work split.  The flattened key space [B*H_kv][S] is cut into P contiguous
+// ranges of L keys, one CTA each (P ~ number of SMs), so every SM gets the
+// same number of keys whatever B, H_kv and S are.  A range can cross KV-head
+// boundaries; each piece (one head, keys [a, b)) is a "segment".  Pass-1
+// partial normalisers and pass-2 candidate lists live in per-(CTA, segment)
+// slots whose number depends on P and B*H_kv only, never on S.
+//
+// Warp 0 issues TMA loads (the group's window queries once per segment, then
+// 128-key tiles through a 4-stage ring), warp 1 owns tensor memory and issues
+// the MMAs from one thread into two 256-column accumulator buffers, so the
+// MMA of tile t+1 runs while tile t is being reduced.  Every mbarrier wait is
+// bounded; a wait that gives up records a timeout in the status word and the
+// CTA drains and returns.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "kvc_device.cuh"
+#include "kvc_internal.cuh"
+#include "kvc_tc.cuh"
+
+namespace kvc {
+namespace scan {
+
+#ifndef KVC_P1_STAGES
+#define KVC_P1_STAGES 4
+#endif
+constexpr int kStages = KVC_P1_STAGES;        // key-tile ring depth of pass 1
+constexpr int kMaxStages = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccStride = 256;          // TMEM columns per accumulator buffer
+constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSegs = 8;
+#ifndef KVC_PREFETCH_TILES
+#define KVC_PREFETCH_TILES 0
+#endif
+constexpr int kPrefetchTiles = KVC_PREFETCH_TILES;   // L2 prefetch distance of the key tiles
+
+struct ScanArgs {
+  int B, H_q, H_kv, S, W, gw, gwp16, n_mb, nq, P, maxseg, pool_k, cap;
+  int64_t L;
+  float c2;                  // log2(e) / sqrt(D)
+  float* part_m;             // pass 1 out: [P*maxseg][gwp16] (log2 units)
+  float* part_z;
+  const float* m_in;         // pass 2: natural-unit m, Z [B][H_q][W] ...
+  const float* z_in;
+  const float* pm_in;        // ... or pass-1 partials
+  const float* pz_in;
+  const float* bias;         // pass 2: per-row -lse2 / c2 [BH][gwp16]
+  float* scores;             // pass 2 out: dense [BH][S] or nullptr
+  uint64_t* cand;            // pass 2 out: [P*maxseg][cap]
+  int* cand_cnt;             // [P*maxseg]
+  int* status;
+};
+
+struct Seg {
+  int bh, a, b;
+};
+
+// Bounded wait; on giving up, flags the CTA and the status word.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 4095u) == 4095u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  record_status(status, kStatusTimeout);
+  return false;
+}
+
+// Bounded wait by a whole warp: only lane 0 polls the barrier (many threads
+// spinning on one mbarrier word slow down the shared-memory traffic of the
+// TMA and the MMAs), then the warp is released together.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Segments of CTA c, in key order.
+__device__ __forceinline__ int cta_segments(const ScanArgs& A, int c, Seg* out) {
+  const int64_t total = (int64_t)A.B * A.H_kv * A.S;
+  const int64_t f0 = (int64_t)c * A.L;
+  const int64_t f1 = min(f0 + A.L, total);
+  if (f0 >= f1) return 0;
+  const int h0 = (int)(f0 / A.S), h1 = (int)((f1 - 1) / A.S);
+  int n = 0;
+  for (int h = h0; h <= h1 && n < kMaxSegs; ++h, ++n) {
+    out[n].bh = h;
+    out[n].a = (int)max((int64_t)0, f0 - (int64_t)h * A.S);
+    out[n].b = (int)min((int64_t)A.S, f1 - (int64_t)h * A.S);
+  }
+  return n;
+}
+
+__device__ __forceinline__ float2 merge_mz(float2 a, float2 b) {
+  if (b.y == 0.f) return a;
+  if (a.y == 0.f) return b;
+  const float m = fmaxf(a.x, b.x);
+  return make_float2(m, a.y * ex2(a.x - m) + b.y * ex2(b.x - m));
+}
+
+// (max, Z) of window row `row` of head bh over all pass-1 slots of the head.
+__device__ __forceinline__ float2 combine_partials(const ScanArgs& A, int bh, int row) {
+  const int64_t S = A.S;
+  const int c_first = (int)(((int64_t)bh * S) / A.L);
+  const int c_last = (int)((((int64_t)bh + 1) * S - 1) / A.L);
+  float2 st = make_float2(-INFINITY, 0.f);
+  for (int c = c_first; c <= c_last; ++c) {
+    const int seg = bh - (int)(((int64_t)c * A.L) / S);
+    const size_t o = ((size_t)c * A.maxseg + seg) * A.gwp16 + row;
+    st = merge_mz(st, make_float2(A.pm_in[o], A.pz_in[o]));
+  }
+  return st;
+}
+
+struct PipeBars {
+  uint64_t full[kMaxStages], empty[kMaxStages], tfull[4], tempty[4], qfull, qempty;
+};
+
+__device__ __forceinline__ void init_pipe_bars(PipeBars* b, int tempty_count, int nst = kStages) {
+  for (int i = 0; i < nst; ++i) {
+    tc::mbar_init(smem_u32(&b->full[i]), 1);
+    tc::mbar_init(smem_u32(&b->empty[i]), 1);
+  }
+  for (int i = 0; i < 4; ++i) {
+    tc::mbar_init(smem_u32(&b->tfull[i]), 1);
+    tc::mbar_init(smem_u32(&b->tempty[i]), tempty_count);
+  }
+  tc::mbar_init(smem_u32(&b->qfull), 1);
+  tc::mbar_init(smem_u32(&b->qempty), 1);
+}
+
+// TMA producer (one thread): per segment the window queries, then the key
+// tiles through a ring of NST stages.
+template <int D, int PASS, int NST = kStages>
+__device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUtensorMap* kmap, PipeBars* bars,
+                         uint32_t sQ, uint32_t sK, volatile int* abort_flag) {
+  constexpr int NKH = D / 64;
+  constexpr uint32_t kTileBytes = kTile * 128 * NKH;
+  const uint32_t q_half = (uint32_t)A.nq * 128;
+  const uint32_t q_bytes = q_half * NKH;
+  const int hw = PASS == 2 ? (A.pool_k - 1) / 2 : 0;
+  Seg segs[kMaxSegs];
+  const int nseg = cta_segments(A, blockIdx.x, segs);
+  const int G = A.H_q / A.H_kv;
+  uint32_t stage = 0, phase = 0, qphase = 0;
+  for (int s = 0; s < nseg; ++s) {
+    const Seg sg = segs[s];
+    if (s > 0) {
+      if (!wait_bar(smem_u32(&bars->qempty), qphase, abort_flag, A.status)) return;
+      qphase ^= 1;
+    }
+    const int b_idx = sg.bh / A.H_kv, hk = sg.bh % A.H_kv;
+    const int qrow = (b_idx * A.H_q + hk * G) * A.W;
+    tc::mbar_arrive_expect_tx(smem_u32(&bars->qfull), q_bytes);
+    for (int kh = 0; kh < NKH; ++kh)
+      tc::tma_load_3d(sQ + kh * q_half, qmap, smem_u32(&bars->qfull), kh * 64, qrow, 0);
+    const int start = sg.a - hw;
+    const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
+    // key tiles run kPrefetchTiles ahead into L2, so the shared-memory ring
+    // only has to cover L2 latency
+    for (int t = 0; t < min(ntiles, kPrefetchTiles); ++t)
+      for (int kh = 0; kh < NKH; ++kh) tc::tma_prefetch_l2_3d(kmap, kh * 64, start + t * kTile, sg.bh);
+    for (int t = 0; t < ntiles; ++t) {
+      if (t + kPrefetchTiles < ntiles)
+        for (int kh = 0; kh < NKH; ++kh)
+          tc::tma_prefetch_l2_3d(kmap, kh * 64, start + (t + kPrefetchTiles) * kTile, sg.bh);
+      if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, A.status)) return;
+      const uint32_t dst = sK + stage * kTileBytes;
+      tc::mbar_arrive_expect_tx(smem_u32(&bars->full[stage]), kTileBytes);
+      for (int kh = 0; kh < NKH; ++kh)
+        tc::tma_load_3d(dst + kh * (kTile * 128), kmap, smem_u32(&bars->full[stage]), kh * 64, start + t * kTile,
+                        sg.bh);
+      if (++stage == NST) { stage = 0; phase ^= 1; }
+    }
+  }
+}
+
+// MMA issuer (one thread).  Pass 1: A = window queries (M = 128 per block),
+// B = key tile (N = 128).  Pass 2: A = key tile (M = 128), B = window queries
+// (N = G*W rounded to 16).  Both operands K-major bf16 in 128-byte swizzle.
+template <int D, int PASS>
+__device__ void mma_issuer(const ScanArgs& A, PipeBars* bars, uint32_t sQ, uint32_t sK, uint32_t tmem,
+                           volatile int* abort_flag) {
+  constexpr int NKH = D / 64;
+  constexpr int KSTEPS = D / 16;
+  constexpr uint32_t kTileBytes = kTile * 128 * NKH;
+  const uint32_t q_half = (uint32_t)A.nq * 128;
+  const int hw = PASS == 2 ? (A.pool_k - 1) / 2 : 0;
+  Seg segs[kMaxSegs];
+  const int nseg = cta_segments(A, blockIdx.x, segs);
+  uint32_t stage = 0, phase = 0, qphase = 0, buf = 0, tphase = 0;
+  const uint32_t idesc = PASS == 1 ? tc::idesc_bf16(128, 128) : tc::idesc_bf16(128, A.gwp16);
+  for (int s = 0; s < nseg; ++s) {
+    const Seg sg = segs[s];
+    if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) return;
+    qphase ^= 1;
+    const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status)) return;
+      if (!wait_bar(smem_u32(&bars->tempty[buf]), tphase ^ 1, abort_flag, A.status)) return;
+      tc::fence_after_sync();
+      const uint32_t kb = sK + stage * kTileBytes;
+      const uint32_t dacc = tmem + buf * kAccStride;
+      if (PASS == 1) {
+        for (int mb = 0; mb < A.n_mb; ++mb) {
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
+            const uint32_t qoff = (ks >> 2) * q_half + mb * (128 * 128) + (ks & 3) * 32;
+            tc::mma_bf16(dacc + mb * 128, tc::desc_sw128(sQ + qoff), tc::desc_sw128(kb + koff), idesc, ks > 0);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
+          const uint32_t qoff = (ks >> 2) * q_half + (ks & 3) * 32;
+          tc::mma_bf16(dacc, tc::desc_sw128(kb + koff), tc::desc_sw128(sQ + qoff), idesc, ks > 0);
+        }
+      }
+      tc::mma_commit(smem_u32(&bars->empty[stage]));
+      tc::mma_commit(smem_u32(&bars->tfull[buf]));
+      if (++stage == kStages) { stage = 0; phase ^= 1; }
+      if (++buf == 2) { buf = 0; tphase ^= 1; }
+    }
+    tc::mma_commit(smem_u32(&bars->qempty));
+  }
+}
+
+// ------------------------------------------------------------- host side
+inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D map over a [d2][d1][d0] bf16 tensor with 128-byte swizzled 64 x box1 boxes.
+inline bool make_map(CUtensorMap* map, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box1) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {64, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline size_t pipe_smem(int D, int nq) {
+  return 1024 + (size_t)nq * 128 * (D / 64) + (size_t)kStages * kTile * 128 * (D / 64);
+}
+
+inline ScanArgs base_args(const ScanPlan& pl, int B, int H_q, int H_kv, int S, int D, int W) {
+  ScanArgs A{};
+  A.B = B;
+  A.H_q = H_q;
+  A.H_kv = H_kv;
+  A.S = S;
+  A.W = W;
+  A.gw = (H_q / H_kv) * W;
+  A.gwp16 = (A.gw + 15) / 16 * 16;
+  A.n_mb = A.gw > 128 ? 2 : 1;
+  A.P = pl.P;
+  A.L = pl.L;
+  A.maxseg = pl.maxseg;
+  A.c2 = kLog2e / sqrtf((float)D);
+  A.status = status_word_ptr();
+  A.pool_k = 1;
+  return A;
+}
+
+}  // namespace scan
+}  // namespace kvc

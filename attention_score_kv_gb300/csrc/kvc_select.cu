@@ -30,13 +30,16 @@ struct SegView {
 };
 
 // Candidate slot of range `part` of head `seg` (mode 1), or -1 past the last
-// scan CTA that touches the head.
+// scan CTA that touches the head.  Scan CTA c_first holds the head's first
+// key (and may start in an earlier head); every later CTA that touches the
+// head starts inside it, so its slot is that CTA's first one.
 __device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int part) {
   const int64_t S = sp.S;
   const int64_t c_first = ((int64_t)seg * S) / sp.L;
   const int64_t c_last = (((int64_t)seg + 1) * S - 1) / sp.L;
   const int64_t c = c_first + part;
   if (c > c_last) return -1;
+  if (part > 0) return c * sp.maxseg;
   return c * sp.maxseg + (seg - (c * sp.L) / S);
 }
 
@@ -73,12 +76,11 @@ __device__ __forceinline__ void entry_at(const SegView& v, const SelParams& sp, 
 
 __device__ __forceinline__ int seg_total(const SegView& v, const SelParams& sp, int seg) {
   if (v.mode == 0) return sp.r_hi - sp.r_lo;
-  int t = 0;
-  for (int p = 0; p < sp.nparts; ++p) {
-    const int64_t slot = cand_slot(sp, seg, p);
-    if (slot < 0) break;
-    t += min(max(v.cand_cnt[slot], 0), v.cap);
-  }
+  const int64_t S = sp.S;
+  const int64_t c_first = ((int64_t)seg * S) / sp.L;
+  const int64_t c_last = (((int64_t)seg + 1) * S - 1) / sp.L;
+  int t = min(max(v.cand_cnt[cand_slot(sp, seg, 0)], 0), v.cap);
+  for (int64_t c = c_first + 1; c <= c_last; ++c) t += min(max(v.cand_cnt[c * sp.maxseg], 0), v.cap);
   return t;
 }
 
@@ -149,17 +151,21 @@ kvc_hist_kernel(SegView v, const __grid_constant__ SelParams sp, int round, uint
   __syncthreads();
   int64_t first;
   const int len = range_len(v, sp, seg, part, &first);
-  for (int i = threadIdx.x; i < len; i += blockDim.x) {
-    uint32_t u;
-    int j;
-    entry_at(v, sp, seg, part, first, i, &u, &j);
-    if (round == 0) {
-      atomicAdd(&sh[u >> 21], 1u);
-    } else if (round == 1) {
-      if ((u >> 21) == prefix) atomicAdd(&sh[(u >> 10) & 2047u], 1u);
-    } else {
-      if ((u >> 10) == prefix) atomicAdd(&sh[u & 1023u], 1u);
+  // Scores of one head share their leading bits, so many keys hit the same
+  // digit: lanes with equal digits are merged into one shared-memory atomic.
+  for (int i0 = 0; i0 < len; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    int bin = -1;
+    if (i < len) {
+      uint32_t u;
+      int j;
+      entry_at(v, sp, seg, part, first, i, &u, &j);
+      if (round == 0) bin = (int)(u >> 21);
+      else if (round == 1) bin = (u >> 21) == prefix ? (int)((u >> 10) & 2047u) : -1;
+      else bin = (u >> 10) == prefix ? (int)(u & 1023u) : -1;
     }
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh[bin], (uint32_t)__popc(peers));
   }
   __syncthreads();
   uint32_t* dst = hseg + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
@@ -250,34 +256,60 @@ kvc_write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t
   __syncthreads();
   int64_t first;
   const int len = range_len(v, sp, seg, part, &first);
-  int written = 0, eq_seen = 0;
-  for (int base = 0; base < len; base += blockDim.x) {
-    const int i = base + threadIdx.x;
+  // each warp owns a contiguous stretch of the range: count it, then write it
+  // in order with ballots; one block-wide exchange places the warps
+  constexpr int kWarps = kSelThreads / 32;
+  __shared__ int s_wgt[kWarps], s_weq[kWarps], s_wout[kWarps], s_weqb[kWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int chunk = (len + kWarps - 1) / kWarps;
+  const int lo = min(len, w * chunk), hi = min(len, lo + chunk);
+  int gtw = 0, eqw = 0;
+  for (int i = lo + lane; i < hi; i += 32) {
+    uint32_t u;
+    int j;
+    entry_at(v, sp, seg, part, first, i, &u, &j);
+    gtw += mode == 2 ? 1 : (u > T);
+    eqw += mode == 2 ? 0 : (u == T);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gtw += __shfl_xor_sync(0xffffffffu, gtw, o);
+    eqw += __shfl_xor_sync(0xffffffffu, eqw, o);
+  }
+  if (lane == 0) { s_wgt[w] = gtw; s_weq[w] = eqw; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ob = out_before, eb = eq_before;
+    for (int q = 0; q < kWarps; ++q) {
+      s_wout[q] = ob;
+      s_weqb[q] = eb;
+      ob += s_wgt[q] + (mode == 2 ? 0 : max(0, min(s_weq[q], need_eq - eb)));
+      eb += s_weq[q];
+    }
+  }
+  __syncthreads();
+  int written = s_wout[w], eq_seen = s_weqb[w];
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
     uint32_t u = 0;
     int j = 0;
-    int is_eq = 0, is_gt = 0;
-    if (i < len) {
+    bool is_gt = false, is_eq = false;
+    if (i < hi) {
       entry_at(v, sp, seg, part, first, i, &u, &j);
-      if (mode == 2) {
-        is_gt = 1;
-      } else {
-        is_gt = u > T;
-        is_eq = u == T;
-      }
+      is_gt = mode == 2 || u > T;
+      is_eq = mode != 2 && u == T;
     }
-    int eq_tot;
-    const int eq_incl = block_inclusive_scan(is_eq, scan, &eq_tot);
-    const int eq_rank = eq_before + eq_seen + eq_incl - is_eq;
-    const int f = is_gt || (is_eq && eq_rank < need_eq);
-    int f_tot;
-    const int f_incl = block_inclusive_scan(f, scan, &f_tot);
+    const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
+    const bool f = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need_eq);
+    const unsigned fb = __ballot_sync(0xffffffffu, f);
     if (f) {
-      const int r = out_before + written + f_incl - 1;
+      const int r = written + __popc(fb & lt);
       if (r < n_take) out[sp.r_lo + r] = j;
       else record_status(status, kStatusSelectMismatch);
     }
-    written += f_tot;
-    eq_seen += eq_tot;
+    written += __popc(fb);
+    eq_seen += __popc(eqb);
   }
 }
 

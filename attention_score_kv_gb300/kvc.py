@@ -15,7 +15,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvc.so")
+# KVC_LIBRARY selects another build of the same library (e.g. one compiled
+# with different tuning flags); default: the in-tree libkvc.so.
+LIB_PATH = os.environ.get("KVC_LIBRARY") or os.path.join(_HERE, "libkvc.so")
 
 KVC_OK = 0
 KVC_ERR_INVALID_ARG = -1
@@ -134,11 +136,10 @@ def kvc_score_pass1_noalloc(q_win, k, B, H_q, H_kv, S, D, W, b_s, m, Z, stream=N
                                         _stream(stream)))
 
 
-def kvc_score_pass2_pool(q_win, k, m, Z, B, H_q, H_kv, S, D, W, b_s, pool_k, scores, ws=None,
-                         ws_bytes=0, stream=None):
+def kvc_score_pass2_pool(q_win, k, m, Z, B, H_q, H_kv, S, D, W, b_s, pool_k, scores, ws, ws_bytes=None,
+                         stream=None):
     _check(_lib.kvc_score_pass2_pool(_ptr(q_win), _ptr(k), _ptr(m), _ptr(Z), B, H_q, H_kv, S, D, W, b_s,
-                                     pool_k, _ptr(scores), _ptr(ws),
-                                     (ws.numel() if ws is not None and not ws_bytes else ws_bytes),
+                                     pool_k, _ptr(scores), _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
                                      _stream(stream)))
 
 

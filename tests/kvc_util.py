@@ -62,7 +62,7 @@ def run_decomposed(K, cfg, inp, K_l, dev="cuda"):
     Z = torch.empty_like(m)
     K.kvc_score_pass1(q, k, B, Hq, Hkv, S, D, W, cfg.b_s, m, Z, ws)
     scores = torch.empty((B, Hkv, S), dtype=torch.float32, device=dev)
-    K.kvc_score_pass2_pool(q, k, m, Z, B, Hq, Hkv, S, D, W, cfg.b_s, cfg.pool_k, scores)
+    K.kvc_score_pass2_pool(q, k, m, Z, B, Hq, Hkv, S, D, W, cfg.b_s, cfg.pool_k, scores, ws)
     k_out, v_out, pos, off = K.retained_outputs(B, Hkv, S, D, K_l, device=dev)
     idx = torch.empty_like(pos)
     K.kvc_select_topk(scores, B, Hkv, S, K_l, cfg.sink, cfg.recent, idx, ws)
