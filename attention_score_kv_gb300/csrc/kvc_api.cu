@@ -147,7 +147,7 @@ bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int
   L->off_part_m = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
   L->off_part_z = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
   L->off_hist = o;     o = align256(o + (size_t)BH * kHistPerSeg * sizeof(uint32_t));
-  L->off_pcnt = o;     o = align256(o + (size_t)BH * parts * sizeof(int2));
+  L->off_pcnt = o;     o = align256(o + (size_t)BH * parts * kSelectSplit * sizeof(int2));
   L->off_cand_cnt = o; o = align256(o + (size_t)L->slots * sizeof(int));
   L->off_cand = o;     o = align256(o + (size_t)L->slots * (size_t)L->cap * sizeof(uint64_t));
   L->total = o;
@@ -327,7 +327,7 @@ int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* 
   if (!layout_ws(B, H_kv, H_kv, 64, 1, kTile, 0, 1, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
   const int BH = B * H_kv;
   sp.nparts = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(2 * (int64_t)num_sms(), BH), max_parts(BH)));
-  if ((rc = check_ws(ws, ws_bytes, L.off_pcnt + (size_t)BH * max_parts(BH) * sizeof(int2)))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, L.off_pcnt + (size_t)BH * max_parts(BH) * kSelectSplit * sizeof(int2)))) return rc;
   char* w = static_cast<char*>(ws);
   return launch_status(launch_select(0, scores, nullptr, nullptr, 0, B, sp, reinterpret_cast<uint32_t*>(w + L.off_hist),
                                      reinterpret_cast<int2*>(w + L.off_pcnt), idx,

@@ -20,6 +20,8 @@ namespace kvc {
 namespace {
 
 constexpr int kSelThreads = 256;
+constexpr int kBatch = 4;   // independent entry loads in flight per thread
+constexpr int kSplit = kSelectSplit;   // CTAs sharing one key range
 
 struct SegView {
   int mode;
@@ -74,16 +76,6 @@ __device__ __forceinline__ void entry_at(const SegView& v, const SelParams& sp, 
   }
 }
 
-__device__ __forceinline__ int seg_total(const SegView& v, const SelParams& sp, int seg) {
-  if (v.mode == 0) return sp.r_hi - sp.r_lo;
-  const int64_t S = sp.S;
-  const int64_t c_first = ((int64_t)seg * S) / sp.L;
-  const int64_t c_last = (((int64_t)seg + 1) * S - 1) / sp.L;
-  int t = min(max(v.cand_cnt[cand_slot(sp, seg, 0)], 0), v.cap);
-  for (int64_t c = c_first + 1; c <= c_last; ++c) t += min(max(v.cand_cnt[c * sp.maxseg], 0), v.cap);
-  return t;
-}
-
 struct FindSmem {
   int scan[32];
   int digit, need;
@@ -99,14 +91,14 @@ __device__ void find_digit(const uint32_t* hist, int nbins, int need, FindSmem* 
   const int hi = nbins - 1 - tid * per;  // this thread covers digits hi, hi-1, ..., hi-per+1
   if (tid == 0) { fs->digit = 0; fs->need = 0; }
   int local = 0;
-  for (int i = 0; i < per; ++i) local += (int)hist[hi - i];
+  for (int i = 0; i < per; ++i) local += (int)__ldcg(&hist[hi - i]);
   int tot;
   const int incl = block_inclusive_scan(local, fs->scan, &tot);
   const int before = incl - local;
   if (before < need && need <= incl) {
     int cum = before;
     for (int i = 0; i < per; ++i) {
-      const int c = (int)hist[hi - i];
+      const int c = (int)__ldcg(&hist[hi - i]);
       if (cum + c >= need) {
         fs->digit = hi - i;
         fs->need = need - cum;
@@ -121,99 +113,136 @@ __device__ void find_digit(const uint32_t* hist, int nbins, int need, FindSmem* 
   __syncthreads();
 }
 
-// Recompute the digits found by earlier rounds for segment `seg`.
-__device__ void replay_rounds(const uint32_t* hist_seg, int rounds, int n_sel, FindSmem* fs,
-                              uint32_t* prefix, int* need) {
-  uint32_t pre = 0;
-  int nd = n_sel, d;
-  if (rounds >= 1) { find_digit(hist_seg, kHist1, nd, fs, &d, &nd); pre = (uint32_t)d; }
-  if (rounds >= 2) { find_digit(hist_seg + kHist1, kHist2, nd, fs, &d, &nd); pre = (pre << 11) | (uint32_t)d; }
-  if (rounds >= 3) { find_digit(hist_seg + kHist1 + kHist2, kHist3, nd, fs, &d, &nd); pre = (pre << 10) | (uint32_t)d; }
-  *prefix = pre;
-  *need = nd;
-}
 
 // Histogram round `round` (0, 1, 2) over one key range.
 __global__ void __launch_bounds__(kSelThreads)
 kvc_hist_kernel(SegView v, const __grid_constant__ SelParams sp, int round, uint32_t* __restrict__ hist) {
-  const int part = blockIdx.x, seg = blockIdx.y, h = seg % sp.H_kv;
+  const int part = blockIdx.x / kSplit, sub = blockIdx.x % kSplit, seg = blockIdx.y, h = seg % sp.H_kv;
   __shared__ uint32_t sh[kHist1];
   __shared__ FindSmem fs;
   const int n_sel = sp.n_sel[h];
-  const int total = seg_total(v, sp, seg);
-  if (n_sel <= 0 || n_sel >= total) return;  // nothing to rank
   uint32_t* hseg = hist + (size_t)seg * kHistPerSeg;
+  SelState* st = reinterpret_cast<SelState*>(hseg + kHistBins);
   uint32_t prefix = 0;
-  int need;
-  replay_rounds(hseg, round, n_sel, &fs, &prefix, &need);
+  int need = 0;
+  if (round > 0) {
+    if (st->mode != 1) return;  // nothing to rank: every CTA of the head leaves
+    prefix = st->prefix;
+    need = st->need;
+  }
   const int nb = round == 2 ? kHist3 : kHist1;
   for (int i = threadIdx.x; i < nb; i += blockDim.x) sh[i] = 0;
   __syncthreads();
   int64_t first;
-  const int len = range_len(v, sp, seg, part, &first);
+  const int plen = range_len(v, sp, seg, part, &first);
+  const int lo = (int)((int64_t)plen * sub / kSplit), len = (int)((int64_t)plen * (sub + 1) / kSplit);
   // Scores of one head share their leading bits, so many keys hit the same
   // digit: lanes with equal digits are merged into one shared-memory atomic.
-  for (int i0 = 0; i0 < len; i0 += blockDim.x) {
-    const int i = i0 + threadIdx.x;
-    int bin = -1;
-    if (i < len) {
-      uint32_t u;
+  // kBatch independent loads per thread are in flight before any is used.
+  for (int i0 = lo; i0 < len; i0 += kBatch * kSelThreads) {
+    uint32_t u[kBatch];
+    bool in[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = i0 + q * kSelThreads + threadIdx.x;
+      in[q] = i < len;
       int j;
-      entry_at(v, sp, seg, part, first, i, &u, &j);
-      if (round == 0) bin = (int)(u >> 21);
-      else if (round == 1) bin = (u >> 21) == prefix ? (int)((u >> 10) & 2047u) : -1;
-      else bin = (u >> 10) == prefix ? (int)(u & 1023u) : -1;
+      u[q] = 0u;
+      if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &j);
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-    if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh[bin], (uint32_t)__popc(peers));
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      int bin = -1;
+      if (in[q]) {
+        if (round == 0) bin = (int)(u[q] >> 21);
+        else if (round == 1) bin = (u[q] >> 21) == prefix ? (int)((u[q] >> 10) & 2047u) : -1;
+        else bin = (u[q] >> 10) == prefix ? (int)(u[q] & 1023u) : -1;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh[bin], (uint32_t)__popc(peers));
+    }
   }
   __syncthreads();
   uint32_t* dst = hseg + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
   for (int i = threadIdx.x; i < nb; i += blockDim.x)
     if (sh[i]) atomicAdd(&dst[i], sh[i]);
+  // the last CTA of this head to finish resolves the round's digit once
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&st->done[round], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (round == 0) {
+    int c = 0;
+    for (int i = threadIdx.x; i < kHist1; i += blockDim.x) c += (int)__ldcg(&dst[i]);
+    int total;
+    block_inclusive_scan(c, fs.scan, &total);
+    if (threadIdx.x == 0) {
+      st->total = total;
+      st->mode = n_sel <= 0 ? 0 : n_sel >= total ? 2 : 1;
+    }
+    if (n_sel <= 0 || n_sel >= total) return;
+  }
+  int d, nd;
+  find_digit(dst, nb, round == 0 ? n_sel : need, &fs, &d, &nd);
+  if (threadIdx.x == 0) {
+    st->prefix = round == 0 ? (uint32_t)d : round == 1 ? (prefix << 11) | (uint32_t)d : (prefix << 10) | (uint32_t)d;
+    st->need = nd;
+  }
 }
 
-// Exact threshold T and the count of keys equal to T still needed.
-// take_all / take_none encode the trivial cases.
-__device__ void threshold(const SegView& v, const SelParams& sp, int seg, const uint32_t* hist,
-                          FindSmem* fs, uint32_t* T, int* need_eq, int* mode) {
-  const int h = seg % sp.H_kv;
-  const int n_sel = sp.n_sel[h];
-  const int total = seg_total(v, sp, seg);
-  if (n_sel <= 0) { *mode = 0; *T = 0; *need_eq = 0; return; }
-  if (n_sel >= total) { *mode = 2; *T = 0; *need_eq = 0; return; }
-  replay_rounds(hist + (size_t)seg * kHistPerSeg, 3, n_sel, fs, T, need_eq);
-  *mode = 1;
+// Exact threshold T and the count of keys equal to T still needed, as left
+// by the histogram rounds.  mode 0: take none, 2: take every candidate.
+__device__ __forceinline__ void threshold(const SelState* st, uint32_t* T, int* need_eq, int* mode, int* total) {
+  *mode = st->mode;
+  *T = st->prefix;
+  *need_eq = st->need;
+  *total = st->total;
 }
 
 // Per range: number of keys scoring above T and exactly T.
 __global__ void __launch_bounds__(kSelThreads)
 kvc_count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
              int2* __restrict__ pcnt) {
-  const int part = blockIdx.x, seg = blockIdx.y;
-  __shared__ FindSmem fs;
+  const int part = blockIdx.x / kSplit, sub = blockIdx.x % kSplit, seg = blockIdx.y;
   __shared__ int scan[32];
   uint32_t T;
-  int need_eq, mode;
-  threshold(v, sp, seg, hist, &fs, &T, &need_eq, &mode);
+  int need_eq, mode, total;
+  threshold(reinterpret_cast<const SelState*>(hist + (size_t)seg * kHistPerSeg + kHistBins), &T, &need_eq, &mode,
+            &total);
   int64_t first;
-  const int len = range_len(v, sp, seg, part, &first);
+  const int plen = range_len(v, sp, seg, part, &first);
+  const int lo = (int)((int64_t)plen * sub / kSplit), len = (int)((int64_t)plen * (sub + 1) / kSplit);
   int gt = 0, eq = 0;
   if (mode == 1) {
-    for (int i = threadIdx.x; i < len; i += blockDim.x) {
-      uint32_t u;
-      int j;
-      entry_at(v, sp, seg, part, first, i, &u, &j);
-      gt += (u > T);
-      eq += (u == T);
+    for (int i0 = lo; i0 < len; i0 += kBatch * kSelThreads) {
+      uint32_t u[kBatch];
+      bool in[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int i = i0 + q * kSelThreads + threadIdx.x;
+        int j;
+        u[q] = 0u;
+        in[q] = i < len;
+        if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &j);
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        gt += (in[q] && u[q] > T);
+        eq += (in[q] && u[q] == T);
+      }
     }
   } else if (mode == 2) {
-    gt = threadIdx.x == 0 ? len : 0;
+    gt = threadIdx.x == 0 ? len - lo : 0;
   }
   int tg, te;
   block_inclusive_scan(gt, scan, &tg);
   block_inclusive_scan(eq, scan, &te);
-  if (threadIdx.x == 0) pcnt[(size_t)seg * sp.nparts + part] = make_int2(tg, te);
+  if (threadIdx.x == 0) pcnt[(size_t)seg * sp.nparts * kSplit + blockIdx.x] = make_int2(tg, te);
 }
 
 // Ordered write of the retained positions of one range; range 0 also writes
@@ -221,55 +250,71 @@ kvc_count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t
 __global__ void __launch_bounds__(kSelThreads)
 kvc_write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
              const int2* __restrict__ pcnt, int32_t* __restrict__ idx, int* status) {
-  const int part = blockIdx.x, seg = blockIdx.y;
+  const int part = blockIdx.x / kSplit, seg = blockIdx.y;
   const int b = seg / sp.H_kv, h = seg % sp.H_kv;
-  __shared__ FindSmem fs;
   __shared__ int scan[32];
   uint32_t T;
-  int need_eq, mode;
-  threshold(v, sp, seg, hist, &fs, &T, &need_eq, &mode);
+  int need_eq, mode, total;
+  threshold(reinterpret_cast<const SelState*>(hist + (size_t)seg * kHistPerSeg + kHistBins), &T, &need_eq, &mode,
+            &total);
   const int n_sel = sp.n_sel[h];
-  const int n_take = mode == 0 ? 0 : mode == 2 ? seg_total(v, sp, seg) : n_sel;
+  const int n_take = mode == 0 ? 0 : mode == 2 ? total : n_sel;
   int32_t* out = idx + (size_t)b * sp.T + sp.off[h];
-  if (part == 0) {
+  if (blockIdx.x == 0) {
     for (int jj = threadIdx.x; jj < sp.r_lo; jj += blockDim.x) out[jj] = jj;
     for (int jj = sp.r_hi + threadIdx.x; jj < sp.S; jj += blockDim.x) out[sp.r_lo + n_take + (jj - sp.r_hi)] = jj;
   }
   if (mode == 0) return;
-  // exclusive prefix over earlier ranges; the ties taken by a range depend on
-  // the running tie count, so one thread walks them in order
+  // exclusive prefix over the earlier sub-ranges of this head (in key order):
+  // a sub-range q takes all its keys above T and, of its ties, as many as
+  // are still needed after the ties of the sub-ranges before it
+  const int nb = blockIdx.x;
+  const int2* pc = pcnt + (size_t)seg * sp.nparts * kSplit;
   int out_before = 0, eq_before = 0;
-  if (threadIdx.x == 0) {
-    int eqb = 0, ob = 0;
-    for (int q = 0; q < part; ++q) {
-      const int2 c = pcnt[(size_t)seg * sp.nparts + q];
-      const int take_eq = mode == 2 ? 0 : max(0, min(c.y, need_eq - eqb));
-      ob += c.x + take_eq;
-      eqb += c.y;
-    }
-    fs.digit = ob;
-    fs.need = eqb;
+  for (int q0 = 0; q0 < nb; q0 += kSelThreads) {
+    const int q = q0 + threadIdx.x;
+    const int2 c = q < nb ? pc[q] : make_int2(0, 0);
+    int tot_eq;
+    const int eq_incl = block_inclusive_scan(c.y, scan, &tot_eq);
+    const int eqb_q = eq_before + eq_incl - c.y;
+    int contrib = c.x + (mode == 2 ? 0 : max(0, min(c.y, need_eq - eqb_q)));
+    int tot_c;
+    block_inclusive_scan(contrib, scan, &tot_c);
+    out_before += tot_c;
+    eq_before += tot_eq;
   }
-  __syncthreads();
-  out_before = fs.digit;
-  eq_before = fs.need;
-  __syncthreads();
   int64_t first;
-  const int len = range_len(v, sp, seg, part, &first);
-  // each warp owns a contiguous stretch of the range: count it, then write it
-  // in order with ballots; one block-wide exchange places the warps
+  const int plen = range_len(v, sp, seg, part, &first);
+  const int sub = blockIdx.x % kSplit;
+  const int slo = (int)((int64_t)plen * sub / kSplit), shi = (int)((int64_t)plen * (sub + 1) / kSplit);
+  // each warp owns a contiguous stretch of the sub-range: count it, then
+  // write it in order with ballots; one block-wide exchange places the warps
   constexpr int kWarps = kSelThreads / 32;
   __shared__ int s_wgt[kWarps], s_weq[kWarps], s_wout[kWarps], s_weqb[kWarps];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int chunk = (len + kWarps - 1) / kWarps;
-  const int lo = min(len, w * chunk), hi = min(len, lo + chunk);
+  const int chunk = (shi - slo + kWarps - 1) / kWarps;
+  const int lo = min(shi, slo + w * chunk), hi = min(shi, lo + chunk);
   int gtw = 0, eqw = 0;
-  for (int i = lo + lane; i < hi; i += 32) {
-    uint32_t u;
-    int j;
-    entry_at(v, sp, seg, part, first, i, &u, &j);
-    gtw += mode == 2 ? 1 : (u > T);
-    eqw += mode == 2 ? 0 : (u == T);
+  if (mode == 2) {
+    gtw = lane == 0 ? hi - lo : 0;
+  } else {
+    for (int i0 = lo; i0 < hi; i0 += 32 * kBatch) {
+      uint32_t u[kBatch];
+      bool in[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int i = i0 + 32 * q + lane;
+        int j;
+        u[q] = 0u;
+        in[q] = i < hi;
+        if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &j);
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        gtw += (in[q] && u[q] > T);
+        eqw += (in[q] && u[q] == T);
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -290,26 +335,33 @@ kvc_write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t
   __syncthreads();
   int written = s_wout[w], eq_seen = s_weqb[w];
   const unsigned lt = (1u << lane) - 1u;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    uint32_t u = 0;
-    int j = 0;
-    bool is_gt = false, is_eq = false;
-    if (i < hi) {
-      entry_at(v, sp, seg, part, first, i, &u, &j);
-      is_gt = mode == 2 || u > T;
-      is_eq = mode != 2 && u == T;
+  for (int b0 = lo; b0 < hi; b0 += 32 * kBatch) {
+    uint32_t u[kBatch];
+    int jj[kBatch];
+    bool in[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = b0 + 32 * q + lane;
+      u[q] = 0u;
+      jj[q] = 0;
+      in[q] = i < hi;
+      if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &jj[q]);
     }
-    const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
-    const bool f = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need_eq);
-    const unsigned fb = __ballot_sync(0xffffffffu, f);
-    if (f) {
-      const int r = written + __popc(fb & lt);
-      if (r < n_take) out[sp.r_lo + r] = j;
-      else record_status(status, kStatusSelectMismatch);
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const bool is_gt = in[q] && (mode == 2 || u[q] > T);
+      const bool is_eq = in[q] && mode != 2 && u[q] == T;
+      const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
+      const bool f = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need_eq);
+      const unsigned fb = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        const int r = written + __popc(fb & lt);
+        if (r < n_take) out[sp.r_lo + r] = jj[q];
+        else record_status(status, kStatusSelectMismatch);
+      }
+      written += __popc(fb);
+      eq_seen += __popc(eqb);
     }
-    written += __popc(fb);
-    eq_seen += __popc(eqb);
   }
 }
 
@@ -358,7 +410,7 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   const int BH = B * sel.H_kv;
   cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)BH * kHistPerSeg * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  dim3 grid(sel.nparts, BH);
+  dim3 grid(sel.nparts * kSplit, BH);
   for (int round = 0; round < 3; ++round) {
     kvc_hist_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, round, hist);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
