@@ -2,12 +2,15 @@
 // log-sum-exp normalisers over the prefix keys, kept as W-length state.
 //
 // A = window queries (two 128-row MMA blocks when G*W > 128), B = 128-key
-// tile.  Eight softmax warps read the accumulators from tensor memory: with
-// two blocks each thread owns one query row and all 128 key columns of a
-// tile; with one block the two warps of a lane quarter split the columns.
-// Each thread keeps a running max (raw dot product units) and the sum of
-// 2^(x - max), x = q.k * log2(e)/sqrt(D), over its segment, then writes the
-// (max * log2(e)/sqrt(D), Z) partial of its row to the segment's slot.
+// tile.  The queries of a segment are copied once from shared into tensor
+// memory and feed every MMA of the segment from there, so the tensor core
+// reads only the key tile from shared memory.  Eight softmax warps read the
+// accumulators from tensor memory: with two blocks each thread owns one
+// query row and all 128 key columns of a tile; with one block the two warps
+// of a lane quarter split the columns.  Each thread keeps a running max (raw
+// dot product units) and the sum of 2^(x - max), x = q.k * log2(e)/sqrt(D),
+// over its segment, then writes the (max * log2(e)/sqrt(D), Z) partial of
+// its row to the segment's slot.
 #include "kvc_scan_common.cuh"
 
 namespace kvc {
@@ -21,43 +24,60 @@ constexpr int kThreads = 64 + kEpiThreads;
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiThreads) : "memory"); }
 
-// Accumulators rotate through four 128-column tensor-memory buffers, one per
-// (tile, 128-row query block) "sub-tile" u: buffer u & 3, completed once per
-// use, so the (u >> 2)-th use of a buffer waits on parity (u >> 2) & 1.  The
-// MMA warp can run two tiles ahead of the softmax warps.
+// Tensor memory: three 128-column accumulator buffers, then the queries
+// (block mb, K-step ks at column kQCol + mb * D/2 + 8 * ks).  Accumulators
+// rotate through the buffers per (tile, 128-row query block) "sub-tile" u:
+// buffer u % 3, completed once per use, so the (u / 3)-th use of a buffer
+// waits on parity (u / 3) & 1.
+constexpr uint32_t kP1Bufs = 3;
+constexpr uint32_t kQCol = kP1Bufs * 128;
+
+__device__ __forceinline__ uint32_t p1_buf(uint32_t u) { return u % kP1Bufs; }
+__device__ __forceinline__ uint32_t p1_parity(uint32_t u) { return (u / kP1Bufs) & 1u; }
+
 template <int D>
-__device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, const Seg* segs, int nseg, uint32_t sQ, uint32_t sK,
-                          uint32_t tmem, volatile int* abort_flag) {
+__device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, uint32_t adrain, const Seg* segs, int nseg,
+                          uint32_t sQ, uint32_t sK, uint32_t tmem, volatile int* abort_flag) {
   constexpr int NKH = D / 64;
   constexpr int KSTEPS = D / 16;
   constexpr uint32_t kTileBytes = kTile * 128 * NKH;
   const uint32_t q_half = (uint32_t)A.nq * 128;
   const uint32_t idesc = tc::idesc_bf16(128, 128);
+  const uint32_t tq = tmem + kQCol;
   uint32_t stage = 0, phase = 0, qphase = 0, u = 0;
   for (int s = 0; s < nseg; ++s) {
     const Seg sg = segs[s];
     if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) return;
     qphase ^= 1;
+    // the previous segment's MMAs must be done reading the old queries
+    if (s > 0 && !wait_bar(adrain, (uint32_t)(s - 1) & 1u, abort_flag, A.status)) return;
+    tc::fence_after_sync();
+    for (int mb = 0; mb < A.n_mb; ++mb)
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const uint32_t qoff = (ks >> 2) * q_half + mb * (128 * 128) + (ks & 3) * 32;
+        tc::tmem_cp_128x256b(tq + mb * (D / 2) + ks * 8, tc::desc_sw128(sQ + qoff));
+      }
+    tc::mma_commit(smem_u32(&bars->qempty));   // shared-memory queries free once copied
     const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
     for (int t = 0; t < ntiles; ++t) {
       if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status)) return;
       const uint32_t kb = sK + stage * kTileBytes;
       for (int mb = 0; mb < A.n_mb; ++mb, ++u) {
-        const uint32_t b = u & 3;
-        if (!wait_bar(smem_u32(&bars->tempty[b]), ((u >> 2) & 1) ^ 1, abort_flag, A.status)) return;
+        const uint32_t b = p1_buf(u);
+        if (!wait_bar(smem_u32(&bars->tempty[b]), p1_parity(u) ^ 1u, abort_flag, A.status)) return;
         tc::fence_after_sync();
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
           const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
-          const uint32_t qoff = (ks >> 2) * q_half + mb * (128 * 128) + (ks & 3) * 32;
-          tc::mma_bf16(tmem + b * 128, tc::desc_sw128(sQ + qoff), tc::desc_sw128(kb + koff), idesc, ks > 0);
+          tc::mma_bf16_ta(tmem + b * 128, tq + mb * (D / 2) + ks * 8, tc::desc_sw128(kb + koff), idesc, ks > 0);
         }
         tc::mma_commit(smem_u32(&bars->tfull[b]));
       }
       tc::mma_commit(smem_u32(&bars->empty[stage]));
       if (++stage == kStages) { stage = 0; phase ^= 1; }
     }
-    tc::mma_commit(smem_u32(&bars->qempty));
+    if (s + 1 < nseg) tc::mma_commit(adrain);
   }
 }
 
@@ -69,6 +89,7 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
   constexpr int NC = NMB == 2 ? 128 : 64;       // accumulator columns per softmax thread
   extern __shared__ uint8_t smem_raw[];
   __shared__ PipeBars bars;
+  __shared__ uint64_t adrain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float2 s_half[128];
@@ -80,6 +101,7 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     init_pipe_bars(&bars, NMB == 2 ? kEpiWarps / 2 : kEpiWarps);
+    tc::mbar_init(smem_u32(&adrain), 1);
     s_abort = 0;
     tc::fence_barrier_init();
   }
@@ -102,7 +124,7 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
     if (lane == 0) {
       Seg segs[kMaxSegs];
       const int nseg = cta_segments(A, blockIdx.x, segs);
-      mma_pass1<D>(A, &bars, segs, nseg, sQ, sK, tmem, &s_abort);
+      mma_pass1<D>(A, &bars, smem_u32(&adrain), segs, nseg, sQ, sK, tmem, &s_abort);
     }
   } else {
     const int e = warp - 2;
@@ -125,8 +147,8 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
       for (int t = 0; t < ntiles; ++t, ++tcount) {
         const uint32_t u = NMB == 2 ? 2 * tcount + mb : tcount;   // this warp's sub-tile
-        const uint32_t buf = u & 3;
-        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), (u >> 2) & 1, &s_abort, A.status)) { ok = false; break; }
+        const uint32_t buf = p1_buf(u);
+        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), p1_parity(u), &s_abort, A.status)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t taddr = tmem + buf * 128 + col0 + ((uint32_t)(quarter * 32) << 16);
         // 64 accumulator columns at a time; the buffer is handed back to the
@@ -169,21 +191,6 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
           }
           if (mrun > -INFINITY) {
             const float nm = -mrun * c2;
-#if KVC_EXP_SCALAR
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f, s6 = 0.f, s7 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-              s0 += ex2(fmaf(v[c], c2, nm));
-              s1 += ex2(fmaf(v[c + 1], c2, nm));
-              s2 += ex2(fmaf(v[c + 2], c2, nm));
-              s3 += ex2(fmaf(v[c + 3], c2, nm));
-              s4 += ex2(fmaf(v[c + 4], c2, nm));
-              s5 += ex2(fmaf(v[c + 5], c2, nm));
-              s6 += ex2(fmaf(v[c + 6], c2, nm));
-              s7 += ex2(fmaf(v[c + 7], c2, nm));
-            }
-            z2.x += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-#else
             const float2 cc = make_float2(c2, c2), nn = make_float2(nm, nm);
             float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
@@ -198,7 +205,6 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
               a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
             }
             z2 = __fadd2_rn(z2, __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3)));
-#endif
           }
         }
       }
