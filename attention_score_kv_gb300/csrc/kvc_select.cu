@@ -6,13 +6,16 @@
 // order like the values; a three-round radix select over those bits (11, 11
 // and 10 bits, each round a histogram of the keys that share the digits found
 // so far) finds the n_sel-th score T and how many keys scoring exactly T are
-// still needed.  Ties at T are taken in ascending index order, which the last
-// two kernels resolve with per-range counts and an ordered block scan.
+// still needed.  Ties at T are taken in ascending index order, resolved with
+// per-unit counts and an ordered block scan.  All of it runs in one
+// cooperative launch whose phases are separated by bounded grid barriers.
 //
 // The keys come either from a dense score array (mode 0) or from the
 // per-range candidate lists of the fused scorer (mode 1, entries
 // (score bits << 32 | index), ascending index within each range, ranges in
 // ascending key order).
+#include <algorithm>
+
 #include "kvc_device.cuh"
 #include "kvc_internal.cuh"
 
@@ -76,244 +79,261 @@ __device__ __forceinline__ void entry_at(const SegView& v, const SelParams& sp, 
   }
 }
 
+// Shared-memory copy of a CTA's first unit: up to kStage entries stay on
+// chip for every round, so only the first round reads them from L2.
+constexpr int kStage = 4096;
+constexpr int kMaxUnits = 8;                  // units one CTA may own
+constexpr uint32_t kBarLimit = 1u << 22;      // polls before a grid barrier gives up
+
 struct FindSmem {
   int scan[32];
-  int digit, need;
+  int digit, need, total;
 };
 
-// Given a histogram (nbins, digit d counts keys whose next digit is d) and the
-// number `need` of keys still to take among them, find the digit holding the
-// need-th largest key and how many keys of that digit are still needed.
-__device__ void find_digit(const uint32_t* hist, int nbins, int need, FindSmem* fs, int* digit_out,
-                           int* need_out) {
+// Given a histogram in global memory (nbins, digit d counts keys whose next
+// digit is d) and the number `need` of keys still to take among them, find
+// the digit holding the need-th largest key, how many keys of that digit are
+// still needed, and the histogram's total.
+__device__ void find_digit(const uint32_t* hist, int nbins, int need, FindSmem* fs, int* digit_out, int* need_out,
+                           int* total_out) {
   const int tid = threadIdx.x;
   const int per = nbins / kSelThreads;   // 8 or 4 bins per thread, highest digits first
   const int hi = nbins - 1 - tid * per;  // this thread covers digits hi, hi-1, ..., hi-per+1
   if (tid == 0) { fs->digit = 0; fs->need = 0; }
+  uint32_t c[8];
   int local = 0;
-  for (int i = 0; i < per; ++i) local += (int)__ldcg(&hist[hi - i]);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = i < per ? __ldcg(&hist[hi - i]) : 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) local += (int)c[i];
   int tot;
   const int incl = block_inclusive_scan(local, fs->scan, &tot);
   const int before = incl - local;
   if (before < need && need <= incl) {
     int cum = before;
-    for (int i = 0; i < per; ++i) {
-      const int c = (int)__ldcg(&hist[hi - i]);
-      if (cum + c >= need) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < per && cum < need && cum + (int)c[i] >= need) {
         fs->digit = hi - i;
         fs->need = need - cum;
-        break;
       }
-      cum += c;
+      cum += (int)c[i];
     }
   }
   __syncthreads();
   *digit_out = fs->digit;
   *need_out = fs->need;
+  *total_out = tot;
   __syncthreads();
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
-// Histogram round `round` (0, 1, 2) over one key range.
-__global__ void __launch_bounds__(kSelThreads)
-kvc_hist_kernel(SegView v, const __grid_constant__ SelParams sp, int round, uint32_t* __restrict__ hist) {
-  const int part = blockIdx.x / kSplit, sub = blockIdx.x % kSplit, seg = blockIdx.y, h = seg % sp.H_kv;
-  __shared__ uint32_t sh[kHist1];
-  __shared__ FindSmem fs;
-  const int n_sel = sp.n_sel[h];
-  uint32_t* hseg = hist + (size_t)seg * kHistPerSeg;
-  SelState* st = reinterpret_cast<SelState*>(hseg + kHistBins);
-  uint32_t prefix = 0;
-  int need = 0;
-  if (round > 0) {
-    if (st->mode != 1) return;  // nothing to rank: every CTA of the head leaves
-    prefix = st->prefix;
-    need = st->need;
+// Grid-wide barrier of a cooperative launch over a monotonic counter that
+// starts at zero: the k-th barrier waits for k * gridDim.x arrivals.  The
+// wait is bounded; giving up records a timeout and makes the CTA return.
+__device__ bool grid_barrier(uint32_t* ctr, uint32_t k, volatile int* s_abort, int* status) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const uint32_t target = k * gridDim.x;
+    uint32_t i = 0;
+    while (ld_acquire_u32(ctr) < target) {
+      if (++i == kBarLimit) {
+        record_status(status, kStatusTimeout);
+        *s_abort = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
   }
+  __syncthreads();
+  return *s_abort == 0;
+}
+
+// One unit of selection work: sub-range `sub` of key range `part` of head
+// `seg`, entries [lo, hi) of the range.
+struct UnitSmem {
+  int seg[kMaxUnits], blk[kMaxUnits], lo[kMaxUnits], hi[kMaxUnits];
+  int mode[kMaxUnits], need[kMaxUnits], total[kMaxUnits];
+  int64_t first[kMaxUnits];
+  uint32_t prefix[kMaxUnits];
+  int n, staged;   // units of this CTA; entries of unit 0 held in shared memory
+};
+
+__device__ __forceinline__ void unit_entry(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui,
+                                           const uint64_t* stage, int i, uint32_t* u, int* j) {
+  if (ui == 0 && i - us.lo[0] < us.staged) {
+    const uint64_t e = stage[i - us.lo[0]];
+    *u = (uint32_t)(e >> 32);
+    *j = (int)(uint32_t)e;
+  } else {
+    entry_at(v, sp, us.seg[ui], 0, us.first[ui], i, u, j);
+  }
+}
+
+// Histogram of round `round` over unit ui into sh, then added to the head's
+// global histogram.  Round 0 also fills the shared-memory copy of unit 0.
+__device__ void unit_hist(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui, int round,
+                          uint64_t* stage, uint32_t* sh, uint32_t* hist) {
   const int nb = round == 2 ? kHist3 : kHist1;
+  const uint32_t prefix = us.prefix[ui];
   for (int i = threadIdx.x; i < nb; i += blockDim.x) sh[i] = 0;
   __syncthreads();
-  int64_t first;
-  const int plen = range_len(v, sp, seg, part, &first);
-  const int lo = (int)((int64_t)plen * sub / kSplit), len = (int)((int64_t)plen * (sub + 1) / kSplit);
-  // Scores of one head share their leading bits, so many keys hit the same
-  // digit: lanes with equal digits are merged into one shared-memory atomic.
-  // kBatch independent loads per thread are in flight before any is used.
-  for (int i0 = lo; i0 < len; i0 += kBatch * kSelThreads) {
+  const int lo = us.lo[ui], hi = us.hi[ui];
+  for (int i0 = lo; i0 < hi; i0 += kBatch * kSelThreads) {
     uint32_t u[kBatch];
+    int jj[kBatch];
     bool in[kBatch];
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
       const int i = i0 + q * kSelThreads + threadIdx.x;
-      in[q] = i < len;
-      int j;
+      in[q] = i < hi;
       u[q] = 0u;
-      if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &j);
+      jj[q] = 0;
+      if (in[q]) {
+        if (round == 0) entry_at(v, sp, us.seg[ui], 0, us.first[ui], i, &u[q], &jj[q]);
+        else unit_entry(v, sp, us, ui, stage, i, &u[q], &jj[q]);
+      }
     }
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
+      const int i = i0 + q * kSelThreads + threadIdx.x;
+      if (round == 0 && ui == 0 && in[q] && i - lo < kStage) stage[i - lo] = ((uint64_t)u[q] << 32) | (uint32_t)jj[q];
       int bin = -1;
       if (in[q]) {
         if (round == 0) bin = (int)(u[q] >> 21);
         else if (round == 1) bin = (u[q] >> 21) == prefix ? (int)((u[q] >> 10) & 2047u) : -1;
         else bin = (u[q] >> 10) == prefix ? (int)(u[q] & 1023u) : -1;
       }
+      // scores of one head share their leading bits, so many lanes hit the
+      // same digit: equal digits are merged into one shared-memory atomic
       const unsigned peers = __match_any_sync(0xffffffffu, bin);
       if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh[bin], (uint32_t)__popc(peers));
     }
   }
   __syncthreads();
-  uint32_t* dst = hseg + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
+  uint32_t* dst = hist + (size_t)us.seg[ui] * kHistPerSeg + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
   for (int i = threadIdx.x; i < nb; i += blockDim.x)
     if (sh[i]) atomicAdd(&dst[i], sh[i]);
-  // the last CTA of this head to finish resolves the round's digit once
-  __shared__ int s_last;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(&st->done[round], 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+}
+
+// Resolve round `round`'s digit of unit ui's head from the global histogram.
+__device__ void unit_resolve(const SelParams& sp, UnitSmem& us, int ui, int round, const uint32_t* hist,
+                             FindSmem* fs) {
+  const uint32_t* hseg = hist + (size_t)us.seg[ui] * kHistPerSeg;
+  int d, nd, tot;
   if (round == 0) {
-    int c = 0;
-    for (int i = threadIdx.x; i < kHist1; i += blockDim.x) c += (int)__ldcg(&dst[i]);
-    int total;
-    block_inclusive_scan(c, fs.scan, &total);
+    const int n_sel = sp.n_sel[us.seg[ui] % sp.H_kv];
+    find_digit(hseg, kHist1, n_sel, fs, &d, &nd, &tot);
     if (threadIdx.x == 0) {
-      st->total = total;
-      st->mode = n_sel <= 0 ? 0 : n_sel >= total ? 2 : 1;
+      us.total[ui] = tot;
+      us.mode[ui] = n_sel <= 0 ? 0 : n_sel >= tot ? 2 : 1;
+      us.prefix[ui] = (uint32_t)d;
+      us.need[ui] = nd;
     }
-    if (n_sel <= 0 || n_sel >= total) return;
+  } else {
+    if (us.mode[ui] != 1) return;
+    const int nb = round == 1 ? kHist2 : kHist3;
+    find_digit(hseg + (round == 1 ? kHist1 : kHist1 + kHist2), nb, us.need[ui], fs, &d, &nd, &tot);
+    if (threadIdx.x == 0) {
+      us.prefix[ui] = (us.prefix[ui] << (round == 1 ? 11 : 10)) | (uint32_t)d;
+      us.need[ui] = nd;
+    }
   }
-  int d, nd;
-  find_digit(dst, nb, round == 0 ? n_sel : need, &fs, &d, &nd);
-  if (threadIdx.x == 0) {
-    st->prefix = round == 0 ? (uint32_t)d : round == 1 ? (prefix << 11) | (uint32_t)d : (prefix << 10) | (uint32_t)d;
-    st->need = nd;
-  }
+  __syncthreads();
 }
 
-// Exact threshold T and the count of keys equal to T still needed, as left
-// by the histogram rounds.  mode 0: take none, 2: take every candidate.
-__device__ __forceinline__ void threshold(const SelState* st, uint32_t* T, int* need_eq, int* mode, int* total) {
-  *mode = st->mode;
-  *T = st->prefix;
-  *need_eq = st->need;
-  *total = st->total;
-}
-
-// Per range: number of keys scoring above T and exactly T.
-__global__ void __launch_bounds__(kSelThreads)
-kvc_count_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
-             int2* __restrict__ pcnt) {
-  const int part = blockIdx.x / kSplit, sub = blockIdx.x % kSplit, seg = blockIdx.y;
-  __shared__ int scan[32];
-  uint32_t T;
-  int need_eq, mode, total;
-  threshold(reinterpret_cast<const SelState*>(hist + (size_t)seg * kHistPerSeg + kHistBins), &T, &need_eq, &mode,
-            &total);
-  int64_t first;
-  const int plen = range_len(v, sp, seg, part, &first);
-  const int lo = (int)((int64_t)plen * sub / kSplit), len = (int)((int64_t)plen * (sub + 1) / kSplit);
+// Keys of unit ui above T and exactly T.
+__device__ int2 unit_count(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui, const uint64_t* stage,
+                           int* scan) {
+  const int mode = us.mode[ui];
+  const uint32_t T = us.prefix[ui];
   int gt = 0, eq = 0;
   if (mode == 1) {
-    for (int i0 = lo; i0 < len; i0 += kBatch * kSelThreads) {
-      uint32_t u[kBatch];
-      bool in[kBatch];
+    for (int i0 = us.lo[ui]; i0 < us.hi[ui]; i0 += kBatch * kSelThreads) {
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const int i = i0 + q * kSelThreads + threadIdx.x;
-        int j;
-        u[q] = 0u;
-        in[q] = i < len;
-        if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &j);
-      }
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        gt += (in[q] && u[q] > T);
-        eq += (in[q] && u[q] == T);
+        if (i < us.hi[ui]) {
+          uint32_t u;
+          int j;
+          unit_entry(v, sp, us, ui, stage, i, &u, &j);
+          gt += u > T;
+          eq += u == T;
+        }
       }
     }
   } else if (mode == 2) {
-    gt = threadIdx.x == 0 ? len - lo : 0;
+    gt = threadIdx.x == 0 ? us.hi[ui] - us.lo[ui] : 0;
   }
   int tg, te;
   block_inclusive_scan(gt, scan, &tg);
   block_inclusive_scan(eq, scan, &te);
-  if (threadIdx.x == 0) pcnt[(size_t)seg * sp.nparts * kSplit + blockIdx.x] = make_int2(tg, te);
+  return make_int2(tg, te);
 }
 
-// Ordered write of the retained positions of one range; range 0 also writes
-// the mandatory positions.
-__global__ void __launch_bounds__(kSelThreads)
-kvc_write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t* __restrict__ hist,
-             const int2* __restrict__ pcnt, int32_t* __restrict__ idx, int* status) {
-  const int part = blockIdx.x / kSplit, seg = blockIdx.y;
+// Ordered write of the retained positions of unit ui; the head's first unit
+// also writes the mandatory positions.
+__device__ void unit_write(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui, const uint64_t* stage,
+                           const int2* pcnt, int32_t* idx, int* scan, int* status) {
+  const int seg = us.seg[ui], blk = us.blk[ui];
   const int b = seg / sp.H_kv, h = seg % sp.H_kv;
-  __shared__ int scan[32];
-  uint32_t T;
-  int need_eq, mode, total;
-  threshold(reinterpret_cast<const SelState*>(hist + (size_t)seg * kHistPerSeg + kHistBins), &T, &need_eq, &mode,
-            &total);
+  const int mode = us.mode[ui], need_eq = us.need[ui], total = us.total[ui];
+  const uint32_t T = us.prefix[ui];
   const int n_sel = sp.n_sel[h];
   const int n_take = mode == 0 ? 0 : mode == 2 ? total : n_sel;
   int32_t* out = idx + (size_t)b * sp.T + sp.off[h];
-  if (blockIdx.x == 0) {
+  if (blk == 0) {
     for (int jj = threadIdx.x; jj < sp.r_lo; jj += blockDim.x) out[jj] = jj;
     for (int jj = sp.r_hi + threadIdx.x; jj < sp.S; jj += blockDim.x) out[sp.r_lo + n_take + (jj - sp.r_hi)] = jj;
   }
   if (mode == 0) return;
-  // exclusive prefix over the earlier sub-ranges of this head (in key order):
-  // a sub-range q takes all its keys above T and, of its ties, as many as
-  // are still needed after the ties of the sub-ranges before it
-  const int nb = blockIdx.x;
+  // exclusive prefix over the earlier units of this head (in key order): a
+  // unit takes all its keys above T and, of its ties, as many as are still
+  // needed after the ties of the units before it
   const int2* pc = pcnt + (size_t)seg * sp.nparts * kSplit;
   int out_before = 0, eq_before = 0;
-  for (int q0 = 0; q0 < nb; q0 += kSelThreads) {
+  for (int q0 = 0; q0 < blk; q0 += kSelThreads) {
     const int q = q0 + threadIdx.x;
-    const int2 c = q < nb ? pc[q] : make_int2(0, 0);
+    int2 c = make_int2(0, 0);
+    if (q < blk) {
+      const long long raw = __ldcg(reinterpret_cast<const long long*>(pc + q));
+      c = make_int2((int)(uint32_t)raw, (int)(raw >> 32));
+    }
     int tot_eq;
     const int eq_incl = block_inclusive_scan(c.y, scan, &tot_eq);
     const int eqb_q = eq_before + eq_incl - c.y;
-    int contrib = c.x + (mode == 2 ? 0 : max(0, min(c.y, need_eq - eqb_q)));
+    const int contrib = c.x + (mode == 2 ? 0 : max(0, min(c.y, need_eq - eqb_q)));
     int tot_c;
     block_inclusive_scan(contrib, scan, &tot_c);
     out_before += tot_c;
     eq_before += tot_eq;
   }
-  int64_t first;
-  const int plen = range_len(v, sp, seg, part, &first);
-  const int sub = blockIdx.x % kSplit;
-  const int slo = (int)((int64_t)plen * sub / kSplit), shi = (int)((int64_t)plen * (sub + 1) / kSplit);
-  // each warp owns a contiguous stretch of the sub-range: count it, then
-  // write it in order with ballots; one block-wide exchange places the warps
+  // each warp owns a contiguous stretch of the unit: count it, then write it
+  // in order with ballots; one block-wide exchange places the warps
   constexpr int kWarps = kSelThreads / 32;
   __shared__ int s_wgt[kWarps], s_weq[kWarps], s_wout[kWarps], s_weqb[kWarps];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int chunk = (shi - slo + kWarps - 1) / kWarps;
-  const int lo = min(shi, slo + w * chunk), hi = min(shi, lo + chunk);
+  const int chunk = (us.hi[ui] - us.lo[ui] + kWarps - 1) / kWarps;
+  const int lo = min(us.hi[ui], us.lo[ui] + w * chunk), hi = min(us.hi[ui], lo + chunk);
   int gtw = 0, eqw = 0;
   if (mode == 2) {
     gtw = lane == 0 ? hi - lo : 0;
   } else {
-    for (int i0 = lo; i0 < hi; i0 += 32 * kBatch) {
-      uint32_t u[kBatch];
-      bool in[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int i = i0 + 32 * q + lane;
-        int j;
-        u[q] = 0u;
-        in[q] = i < hi;
-        if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &j);
-      }
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        gtw += (in[q] && u[q] > T);
-        eqw += (in[q] && u[q] == T);
-      }
+    for (int i = lo + lane; i < hi; i += 32) {
+      uint32_t u;
+      int j;
+      unit_entry(v, sp, us, ui, stage, i, &u, &j);
+      gtw += u > T;
+      eqw += u == T;
     }
   }
 #pragma unroll
@@ -335,34 +355,79 @@ kvc_write_kernel(SegView v, const __grid_constant__ SelParams sp, const uint32_t
   __syncthreads();
   int written = s_wout[w], eq_seen = s_weqb[w];
   const unsigned lt = (1u << lane) - 1u;
-  for (int b0 = lo; b0 < hi; b0 += 32 * kBatch) {
-    uint32_t u[kBatch];
-    int jj[kBatch];
-    bool in[kBatch];
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int i = b0 + 32 * q + lane;
-      u[q] = 0u;
-      jj[q] = 0;
-      in[q] = i < hi;
-      if (in[q]) entry_at(v, sp, seg, part, first, i, &u[q], &jj[q]);
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    uint32_t u = 0u;
+    int j = 0;
+    const bool in = i < hi;
+    if (in) unit_entry(v, sp, us, ui, stage, i, &u, &j);
+    const bool is_gt = in && (mode == 2 || u > T);
+    const bool is_eq = in && mode != 2 && u == T;
+    const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
+    const bool f = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need_eq);
+    const unsigned fb = __ballot_sync(0xffffffffu, f);
+    if (f) {
+      const int r = written + __popc(fb & lt);
+      if (r < n_take) out[sp.r_lo + r] = j;
+      else record_status(status, kStatusSelectMismatch);
     }
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const bool is_gt = in[q] && (mode == 2 || u[q] > T);
-      const bool is_eq = in[q] && mode != 2 && u[q] == T;
-      const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
-      const bool f = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need_eq);
-      const unsigned fb = __ballot_sync(0xffffffffu, f);
-      if (f) {
-        const int r = written + __popc(fb & lt);
-        if (r < n_take) out[sp.r_lo + r] = jj[q];
-        else record_status(status, kStatusSelectMismatch);
-      }
-      written += __popc(fb);
-      eq_seen += __popc(eqb);
+    written += __popc(fb);
+    eq_seen += __popc(eqb);
+  }
+  __syncthreads();
+}
+
+// The whole selection in one cooperative launch.  Each CTA owns up to
+// kMaxUnits units (sub-ranges of one head's key ranges).  Phases, separated
+// by grid barriers: three radix histogram rounds (each CTA resolves the
+// previous round's digit of its own heads from the global histogram), the
+// per-unit counts above and at the threshold, and the ordered write.
+__global__ void __launch_bounds__(kSelThreads)
+kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int n_units, uint32_t* __restrict__ hist,
+                  int2* __restrict__ pcnt, int32_t* __restrict__ idx, int* status) {
+  __shared__ uint32_t sh[kHist1];
+  __shared__ uint64_t stage[kStage];
+  __shared__ FindSmem fs;
+  __shared__ UnitSmem us;
+  __shared__ volatile int s_abort;
+  uint32_t* bar = hist + kHistBins;   // head 0's state word: the barrier counter
+  const int per_head = sp.nparts * kSplit;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    int n = 0;
+    for (int u = blockIdx.x; u < n_units && n < kMaxUnits; u += gridDim.x, ++n) {
+      const int seg = u / per_head, blk = u % per_head;
+      const int part = blk / kSplit, sub = blk % kSplit;
+      int64_t first;
+      const int plen = range_len(v, sp, seg, part, &first);
+      us.seg[n] = seg;
+      us.blk[n] = blk;
+      us.first[n] = first;
+      us.lo[n] = (int)((int64_t)plen * sub / kSplit);
+      us.hi[n] = (int)((int64_t)plen * (sub + 1) / kSplit);
+      us.prefix[n] = 0;
+    }
+    us.n = n;
+    us.staged = 0;
+  }
+  __syncthreads();
+  const int nu = us.n;
+  for (int ui = 0; ui < nu; ++ui) unit_hist(v, sp, us, ui, 0, stage, sh, hist);
+  if (threadIdx.x == 0 && nu > 0) us.staged = min(us.hi[0] - us.lo[0], kStage);
+  for (int round = 1; round <= 3; ++round) {
+    if (!grid_barrier(bar, (uint32_t)round, &s_abort, status)) return;
+    for (int ui = 0; ui < nu; ++ui) {
+      unit_resolve(sp, us, ui, round - 1, hist, &fs);
+      if (round < 3 && us.mode[ui] == 1) unit_hist(v, sp, us, ui, round, stage, sh, hist);
     }
   }
+  // us.prefix is now the threshold T and us.need the ties at T still needed
+  for (int ui = 0; ui < nu; ++ui) {
+    const int2 c = unit_count(v, sp, us, ui, stage, fs.scan);
+    if (threadIdx.x == 0) pcnt[(size_t)us.seg[ui] * per_head + us.blk[ui]] = c;
+  }
+  if (!grid_barrier(bar, 4u, &s_abort, status)) return;
+  for (int ui = 0; ui < nu; ++ui) unit_write(v, sp, us, ui, stage, pcnt, idx, fs.scan, status);
 }
 
 // Gather retained rows: one 16-byte vector per lane, D/8 lanes per row.
@@ -410,15 +475,22 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   const int BH = B * sel.H_kv;
   cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)BH * kHistPerSeg * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  dim3 grid(sel.nparts * kSplit, BH);
-  for (int round = 0; round < 3; ++round) {
-    kvc_hist_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, round, hist);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  kvc_count_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kvc_write_kernel<<<grid, kSelThreads, 0, st>>>(v, sel, hist, pcnt, idx, status_word_ptr());
-  note_launches(5);
+  int n_units = sel.nparts * kSplit * BH;
+  static int occ[64] = {0};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (occ[dev] == 0 &&
+      (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[dev], kvc_select_kernel, kSelThreads, 0)) != cudaSuccess)
+    return e;
+  const int grid = std::min(n_units, std::max(occ[dev], 1) * num_sms());
+  if ((int64_t)grid * kMaxUnits < n_units) return cudaErrorInvalidConfiguration;
+  int* status = status_word_ptr();
+  void* args[] = {&v, const_cast<SelParams*>(&sel), &n_units, &hist, &pcnt, &idx, &status};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kvc_select_kernel), dim3(grid), dim3(kSelThreads), args,
+                                  0, st);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
