@@ -7,8 +7,8 @@
 // and 10 bits, each round a histogram of the keys that share the digits found
 // so far) finds the n_sel-th score T and how many keys scoring exactly T are
 // still needed.  Ties at T are taken in ascending index order, resolved with
-// per-unit counts and an ordered block scan.  All of it runs in one
-// cooperative launch whose phases are separated by bounded grid barriers.
+// per-warp counts and an ordered ballot write.  All of it runs in one launch
+// with one thread-block cluster per head.
 //
 // The keys come either from a dense score array (mode 0) or from the
 // per-range candidate lists of the fused scorer (mode 1, entries
@@ -21,10 +21,6 @@
 
 namespace kvc {
 namespace {
-
-constexpr int kSelThreads = 256;
-constexpr int kBatch = 4;   // independent entry loads in flight per thread
-constexpr int kSplit = kSelectSplit;   // CTAs sharing one key range
 
 struct SegView {
   int mode;
@@ -48,290 +44,280 @@ __device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int p
   return c * sp.maxseg + (seg - (c * sp.L) / S);
 }
 
-// Number of entries of range `part` of head `seg`; for mode 0 also the first
-// key index of the range, for mode 1 the slot.
-__device__ __forceinline__ int range_len(const SegView& v, const SelParams& sp, int seg, int part,
-                                         int64_t* first) {
-  if (v.mode == 0) {
-    const int ncand = sp.r_hi - sp.r_lo;
-    const int per = (ncand + sp.nparts - 1) / sp.nparts;
-    const int lo = part * per;
-    const int hi = min(ncand, lo + per);
-    *first = sp.r_lo + lo;
-    return max(0, hi - lo);
-  }
-  const int64_t slot = cand_slot(sp, seg, part);
-  *first = slot;
-  return slot < 0 ? 0 : min(max(v.cand_cnt[slot], 0), v.cap);
+// One thread-block cluster per (b, KV head).  The head's entries are cut
+// into kCl contiguous shares, one per CTA, and each share is copied once
+// into that CTA's shared memory (up to kStageC entries; the rest, if any, is
+// re-read from global memory in every round).  The radix rounds, the counts
+// and the ordered write then run on chip: per-CTA histograms are summed by
+// reading the other CTAs' shared memory, and hardware cluster barriers
+// separate the phases, so no CTA waits on anything outside its cluster.
+constexpr int kMaxCl = 8;               // CTAs per head at most (portable cluster size)
+constexpr int kClThreads = 512;
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kStageC = 16384;          // entries per CTA kept in shared memory
+constexpr int kCopyBatch = 8;
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 
-__device__ __forceinline__ void entry_at(const SegView& v, const SelParams& sp, int seg, int part,
-                                         int64_t first, int i, uint32_t* u, int* j) {
-  (void)part;
-  if (v.mode == 0) {
-    *j = (int)first + i;
-    uint32_t bits = __float_as_uint(v.scores[(size_t)seg * sp.S + first + i]);
-    *u = (bits == 0x80000000u) ? 0u : bits;
-  } else {
-    const uint64_t e = v.cand[(size_t)first * v.cap + i];
-    *u = (uint32_t)(e >> 32);
-    *j = (int)(uint32_t)e;
-  }
-}
-
-// Shared-memory copy of a CTA's first unit: up to kStage entries stay on
-// chip for every round, so only the first round reads them from L2.
-constexpr int kStage = 4096;
-constexpr int kMaxUnits = 8;                  // units one CTA may own
-constexpr uint32_t kBarLimit = 1u << 22;      // polls before a grid barrier gives up
-
-struct FindSmem {
+struct __align__(16) ClSmem {
+  uint32_t hist[kHist1 + kHist2 + kHist3];   // this CTA's histogram of each round
+  uint32_t red[kHist1 + kHist2 + kHist3];    // cluster sums of the bins this CTA owns
   int scan[32];
-  int digit, need, total;
+  int digit, need;
+  int wgt[kClWarps], weq[kClWarps], wout[kClWarps], weqb[kClWarps];
+  int cta_gt, cta_eq;                        // this CTA's keys above / at the threshold
 };
 
-// Given a histogram in global memory (nbins, digit d counts keys whose next
-// digit is d) and the number `need` of keys still to take among them, find
-// the digit holding the need-th largest key, how many keys of that digit are
-// still needed, and the histogram's total.
-__device__ void find_digit(const uint32_t* hist, int nbins, int need, FindSmem* fs, int* digit_out, int* need_out,
-                           int* total_out) {
-  const int tid = threadIdx.x;
-  const int per = nbins / kSelThreads;   // 8 or 4 bins per thread, highest digits first
-  const int hi = nbins - 1 - tid * per;  // this thread covers digits hi, hi-1, ..., hi-per+1
-  if (tid == 0) { fs->digit = 0; fs->need = 0; }
-  uint32_t c[8];
-  int local = 0;
+// The head's entries in key order: mode 0 the dense scores of the
+// non-mandatory keys, mode 1 the concatenated candidate lists of its key
+// ranges (pref = exclusive prefix of the list lengths).
+struct HeadView {
+  const SegView* v;
+  const SelParams* sp;
+  int seg;
+  const int* pref;
+  int nparts;
+};
+
+__device__ __forceinline__ uint64_t head_entry(const HeadView& hv, int f) {
+  if (hv.v->mode == 0) {
+    const int j = hv.sp->r_lo + f;
+    uint32_t bits = __float_as_uint(hv.v->scores[(size_t)hv.seg * hv.sp->S + j]);
+    bits = (bits == 0x80000000u) ? 0u : bits;
+    return ((uint64_t)bits << 32) | (uint32_t)j;
+  }
+  int lo = 0, hi = hv.nparts - 1;   // last part whose list starts at or before f
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (hv.pref[mid] <= f) lo = mid; else hi = mid - 1;
+  }
+  const int64_t slot = cand_slot(*hv.sp, hv.seg, lo);
+  return hv.v->cand[(size_t)slot * hv.v->cap + (f - hv.pref[lo])];
+}
+
+// Entry f0 + i of this CTA's share (n entries).
+__device__ __forceinline__ uint64_t share_entry(const HeadView& hv, const uint64_t* stage, int f0, int n, int i) {
+  return (n <= kStageC || i < kStageC) ? stage[i] : head_entry(hv, f0 + i);
+}
+
+__device__ __forceinline__ int radix_bin(uint32_t u, int round, uint32_t prefix) {
+  if (round == 0) return (int)(u >> 21);
+  if (round == 1) return (u >> 21) == prefix ? (int)((u >> 10) & 2047u) : -1;
+  return (u >> 10) == prefix ? (int)(u & 1023u) : -1;
+}
+
+// This CTA's histogram of round `round` over its share.
+__device__ void cl_hist(const HeadView& hv, const uint64_t* stage, int f0, int n, int round, uint32_t prefix,
+                        uint32_t* h) {
+  for (int i0 = 0; i0 < n; i0 += kClThreads) {
+    const int i = i0 + threadIdx.x;
+    int bin = -1;
+    if (i < n) bin = radix_bin((uint32_t)(share_entry(hv, stage, f0, n, i) >> 32), round, prefix);
+    // scores of one head share their leading bits, so many lanes hit the
+    // same digit: equal digits are merged into one shared-memory atomic
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  }
+}
+
+// Sum round `round`'s histograms over the cluster and find the digit that
+// holds the need-th largest key and how many keys of that digit are needed.
+// CTA r owns bin slice r: it adds that slice over the cluster (16-byte
+// remote loads) into its `red` array; after a cluster barrier every CTA
+// reads the summed histogram from the owners and scans it.
+template <int kCl>
+__device__ void cl_resolve(ClSmem* cs, int round, int need, int* digit, int* need_out) {
+  const int nbins = round == 2 ? kHist3 : kHist1;
+  const int base = round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2;
+  const int slice = nbins / kCl;                // a multiple of 4
+  const uint32_t rank = cluster_rank();
+  for (int q = threadIdx.x; q < slice / 4; q += kClThreads) {
+    const int bin = base + (int)rank * slice + 4 * q;
+    uint4 t[kCl];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = i < per ? __ldcg(&hist[hi - i]) : 0u;
+    for (int r = 0; r < kCl; ++r) t[r] = ld_dsmem_v4(dsmem_addr(&cs->hist[bin], (uint32_t)r));
+    uint4 acc = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) local += (int)c[i];
+    for (int r = 0; r < kCl; ++r) {
+      acc.x += t[r].x;
+      acc.y += t[r].y;
+      acc.z += t[r].z;
+      acc.w += t[r].w;
+    }
+    *reinterpret_cast<uint4*>(&cs->red[bin]) = acc;
+  }
+  cluster_sync_all();
+  // thread t holds bins b0 .. b0+3, b0 = nbins - 4(t+1): highest digits first
+  const int b0 = nbins - 4 * ((int)threadIdx.x + 1);
+  uint32_t c[4] = {0u, 0u, 0u, 0u};
+  if (b0 >= 0) {
+    const uint4 t = ld_dsmem_v4(dsmem_addr(&cs->red[base + b0], (uint32_t)(b0 / slice)));
+    c[0] = t.w;
+    c[1] = t.z;
+    c[2] = t.y;
+    c[3] = t.x;
+  }
+  const int hi = b0 + 3;
+  const int local = (int)(c[0] + c[1] + c[2] + c[3]);
+  if (threadIdx.x == 0) { cs->digit = 0; cs->need = 0; }
   int tot;
-  const int incl = block_inclusive_scan(local, fs->scan, &tot);
+  const int incl = block_inclusive_scan(local, cs->scan, &tot);
   const int before = incl - local;
-  if (before < need && need <= incl) {
+  if (b0 >= 0 && before < need && need <= incl) {
     int cum = before;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < per && cum < need && cum + (int)c[i] >= need) {
-        fs->digit = hi - i;
-        fs->need = need - cum;
+    for (int i = 0; i < 4; ++i) {
+      if (cum < need && cum + (int)c[i] >= need) {
+        cs->digit = hi - i;
+        cs->need = need - cum;
       }
       cum += (int)c[i];
     }
   }
   __syncthreads();
-  *digit_out = fs->digit;
-  *need_out = fs->need;
-  *total_out = tot;
+  *digit = cs->digit;
+  *need_out = cs->need;
   __syncthreads();
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
+template <int kCl>
+__global__ void __launch_bounds__(kClThreads, 1)
+kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int32_t* __restrict__ idx, int* status) {
+  extern __shared__ __align__(16) uint8_t cl_dyn[];
+  uint64_t* stage = reinterpret_cast<uint64_t*>(cl_dyn);
+  int* pref = reinterpret_cast<int*>(cl_dyn + (size_t)kStageC * sizeof(uint64_t));
+  __shared__ ClSmem cs;
+  const int seg = blockIdx.x / kCl;
+  const int rank = (int)cluster_rank();
+  const int b = seg / sp.H_kv, h = seg % sp.H_kv;
+  const int n_sel = sp.n_sel[h];
+  const int nparts = v.mode == 0 ? 1 : sp.nparts;
 
-// Grid-wide barrier of a cooperative launch over a monotonic counter that
-// starts at zero: the k-th barrier waits for k * gridDim.x arrivals.  The
-// wait is bounded; giving up records a timeout and makes the CTA return.
-__device__ bool grid_barrier(uint32_t* ctr, uint32_t k, volatile int* s_abort, int* status) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
-    const uint32_t target = k * gridDim.x;
-    uint32_t i = 0;
-    while (ld_acquire_u32(ctr) < target) {
-      if (++i == kBarLimit) {
-        record_status(status, kStatusTimeout);
-        *s_abort = 1;
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  return *s_abort == 0;
-}
-
-// One unit of selection work: sub-range `sub` of key range `part` of head
-// `seg`, entries [lo, hi) of the range.
-struct UnitSmem {
-  int seg[kMaxUnits], blk[kMaxUnits], lo[kMaxUnits], hi[kMaxUnits];
-  int mode[kMaxUnits], need[kMaxUnits], total[kMaxUnits];
-  int64_t first[kMaxUnits];
-  uint32_t prefix[kMaxUnits];
-  int n, staged;   // units of this CTA; entries of unit 0 held in shared memory
-};
-
-__device__ __forceinline__ void unit_entry(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui,
-                                           const uint64_t* stage, int i, uint32_t* u, int* j) {
-  if (ui == 0 && i - us.lo[0] < us.staged) {
-    const uint64_t e = stage[i - us.lo[0]];
-    *u = (uint32_t)(e >> 32);
-    *j = (int)(uint32_t)e;
+  for (int i = threadIdx.x; i < kHist1 + kHist2 + kHist3; i += kClThreads) cs.hist[i] = 0u;
+  // list lengths and their exclusive prefix (mode 1), else the dense range
+  int E;
+  if (v.mode == 0) {
+    E = sp.r_hi - sp.r_lo;
+    if (threadIdx.x == 0) pref[0] = 0;
   } else {
-    entry_at(v, sp, us.seg[ui], 0, us.first[ui], i, u, j);
-  }
-}
-
-// Histogram of round `round` over unit ui into sh, then added to the head's
-// global histogram.  Round 0 also fills the shared-memory copy of unit 0.
-__device__ void unit_hist(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui, int round,
-                          uint64_t* stage, uint32_t* sh, uint32_t* hist) {
-  const int nb = round == 2 ? kHist3 : kHist1;
-  const uint32_t prefix = us.prefix[ui];
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) sh[i] = 0;
-  __syncthreads();
-  const int lo = us.lo[ui], hi = us.hi[ui];
-  for (int i0 = lo; i0 < hi; i0 += kBatch * kSelThreads) {
-    uint32_t u[kBatch];
-    int jj[kBatch];
-    bool in[kBatch];
-#pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int i = i0 + q * kSelThreads + threadIdx.x;
-      in[q] = i < hi;
-      u[q] = 0u;
-      jj[q] = 0;
-      if (in[q]) {
-        if (round == 0) entry_at(v, sp, us.seg[ui], 0, us.first[ui], i, &u[q], &jj[q]);
-        else unit_entry(v, sp, us, ui, stage, i, &u[q], &jj[q]);
+    int carry = 0;
+    for (int p0 = 0; p0 < nparts; p0 += kClThreads) {
+      const int p = p0 + threadIdx.x;
+      int len = 0;
+      if (p < nparts) {
+        const int64_t slot = cand_slot(sp, seg, p);
+        len = slot < 0 ? 0 : min(max(v.cand_cnt[slot], 0), v.cap);
       }
+      int tot;
+      const int incl = block_inclusive_scan(len, cs.scan, &tot);
+      if (p < nparts) pref[p] = carry + incl - len;
+      carry += tot;
     }
+    E = carry;
+  }
+  __syncthreads();
+  HeadView hv{&v, &sp, seg, pref, nparts};
+  const int f0 = (int)((int64_t)E * rank / kCl), f1 = (int)((int64_t)E * (rank + 1) / kCl);
+  const int n = f1 - f0;
+  const int mode = n_sel <= 0 ? 0 : n_sel >= E ? 2 : 1;
+
+  // copy this CTA's share into shared memory, list by list
+  if (mode != 0) {
+    const int ns = min(n, kStageC);
+    if (v.mode == 0) {
+      for (int i0 = 0; i0 < ns; i0 += kCopyBatch * kClThreads) {
+        uint64_t t[kCopyBatch];
 #pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int i = i0 + q * kSelThreads + threadIdx.x;
-      if (round == 0 && ui == 0 && in[q] && i - lo < kStage) stage[i - lo] = ((uint64_t)u[q] << 32) | (uint32_t)jj[q];
-      int bin = -1;
-      if (in[q]) {
-        if (round == 0) bin = (int)(u[q] >> 21);
-        else if (round == 1) bin = (u[q] >> 21) == prefix ? (int)((u[q] >> 10) & 2047u) : -1;
-        else bin = (u[q] >> 10) == prefix ? (int)(u[q] & 1023u) : -1;
+        for (int q = 0; q < kCopyBatch; ++q) {
+          const int i = i0 + q * kClThreads + threadIdx.x;
+          t[q] = i < ns ? head_entry(hv, f0 + i) : 0ull;
+        }
+#pragma unroll
+        for (int q = 0; q < kCopyBatch; ++q) {
+          const int i = i0 + q * kClThreads + threadIdx.x;
+          if (i < ns) stage[i] = t[q];
+        }
       }
-      // scores of one head share their leading bits, so many lanes hit the
-      // same digit: equal digits are merged into one shared-memory atomic
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh[bin], (uint32_t)__popc(peers));
-    }
-  }
-  __syncthreads();
-  uint32_t* dst = hist + (size_t)us.seg[ui] * kHistPerSeg + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
-  for (int i = threadIdx.x; i < nb; i += blockDim.x)
-    if (sh[i]) atomicAdd(&dst[i], sh[i]);
-  __syncthreads();
-}
-
-// Resolve round `round`'s digit of unit ui's head from the global histogram.
-__device__ void unit_resolve(const SelParams& sp, UnitSmem& us, int ui, int round, const uint32_t* hist,
-                             FindSmem* fs) {
-  const uint32_t* hseg = hist + (size_t)us.seg[ui] * kHistPerSeg;
-  int d, nd, tot;
-  if (round == 0) {
-    const int n_sel = sp.n_sel[us.seg[ui] % sp.H_kv];
-    find_digit(hseg, kHist1, n_sel, fs, &d, &nd, &tot);
-    if (threadIdx.x == 0) {
-      us.total[ui] = tot;
-      us.mode[ui] = n_sel <= 0 ? 0 : n_sel >= tot ? 2 : 1;
-      us.prefix[ui] = (uint32_t)d;
-      us.need[ui] = nd;
-    }
-  } else {
-    if (us.mode[ui] != 1) return;
-    const int nb = round == 1 ? kHist2 : kHist3;
-    find_digit(hseg + (round == 1 ? kHist1 : kHist1 + kHist2), nb, us.need[ui], fs, &d, &nd, &tot);
-    if (threadIdx.x == 0) {
-      us.prefix[ui] = (us.prefix[ui] << (round == 1 ? 11 : 10)) | (uint32_t)d;
-      us.need[ui] = nd;
-    }
-  }
-  __syncthreads();
-}
-
-// Keys of unit ui above T and exactly T.
-__device__ int2 unit_count(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui, const uint64_t* stage,
-                           int* scan) {
-  const int mode = us.mode[ui];
-  const uint32_t T = us.prefix[ui];
-  int gt = 0, eq = 0;
-  if (mode == 1) {
-    for (int i0 = us.lo[ui]; i0 < us.hi[ui]; i0 += kBatch * kSelThreads) {
+    } else {
+      for (int p = 0; p < nparts; ++p) {
+        const int a = max(f0, pref[p]);
+        const int e = min(f0 + ns, p + 1 < nparts ? pref[p + 1] : E);
+        if (a >= e) continue;
+        const uint64_t* src = v.cand + (size_t)cand_slot(sp, seg, p) * v.cap - pref[p];
+        // kCopyBatch independent loads in flight per thread
+        for (int f = a + threadIdx.x; f < e; f += kCopyBatch * kClThreads) {
+          uint64_t t[kCopyBatch];
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) {
-        const int i = i0 + q * kSelThreads + threadIdx.x;
-        if (i < us.hi[ui]) {
-          uint32_t u;
-          int j;
-          unit_entry(v, sp, us, ui, stage, i, &u, &j);
-          gt += u > T;
-          eq += u == T;
+          for (int q = 0; q < kCopyBatch; ++q) {
+            const int ff = f + q * kClThreads;
+            t[q] = ff < e ? __ldg(reinterpret_cast<const unsigned long long*>(src + ff)) : 0ull;
+          }
+#pragma unroll
+          for (int q = 0; q < kCopyBatch; ++q) {
+            const int ff = f + q * kClThreads;
+            if (ff < e) stage[ff - f0] = t[q];
+          }
         }
       }
     }
-  } else if (mode == 2) {
-    gt = threadIdx.x == 0 ? us.hi[ui] - us.lo[ui] : 0;
   }
-  int tg, te;
-  block_inclusive_scan(gt, scan, &tg);
-  block_inclusive_scan(eq, scan, &te);
-  return make_int2(tg, te);
-}
+  __syncthreads();
 
-// Ordered write of the retained positions of unit ui; the head's first unit
-// also writes the mandatory positions.
-__device__ void unit_write(const SegView& v, const SelParams& sp, const UnitSmem& us, int ui, const uint64_t* stage,
-                           const int2* pcnt, int32_t* idx, int* scan, int* status) {
-  const int seg = us.seg[ui], blk = us.blk[ui];
-  const int b = seg / sp.H_kv, h = seg % sp.H_kv;
-  const int mode = us.mode[ui], need_eq = us.need[ui], total = us.total[ui];
-  const uint32_t T = us.prefix[ui];
-  const int n_sel = sp.n_sel[h];
-  const int n_take = mode == 0 ? 0 : mode == 2 ? total : n_sel;
-  int32_t* out = idx + (size_t)b * sp.T + sp.off[h];
-  if (blk == 0) {
-    for (int jj = threadIdx.x; jj < sp.r_lo; jj += blockDim.x) out[jj] = jj;
-    for (int jj = sp.r_hi + threadIdx.x; jj < sp.S; jj += blockDim.x) out[sp.r_lo + n_take + (jj - sp.r_hi)] = jj;
-  }
-  if (mode == 0) return;
-  // exclusive prefix over the earlier units of this head (in key order): a
-  // unit takes all its keys above T and, of its ties, as many as are still
-  // needed after the ties of the units before it
-  const int2* pc = pcnt + (size_t)seg * sp.nparts * kSplit;
-  int out_before = 0, eq_before = 0;
-  for (int q0 = 0; q0 < blk; q0 += kSelThreads) {
-    const int q = q0 + threadIdx.x;
-    int2 c = make_int2(0, 0);
-    if (q < blk) {
-      const long long raw = __ldcg(reinterpret_cast<const long long*>(pc + q));
-      c = make_int2((int)(uint32_t)raw, (int)(raw >> 32));
+  // radix rounds: T = the n_sel-th largest score bits, need_eq = ties at T to take
+  uint32_t T = 0u;
+  int need_eq = 0;
+  if (mode == 1) {
+    uint32_t prefix = 0u;
+    int need = n_sel;
+    for (int round = 0; round < 3; ++round) {
+      uint32_t* hr = cs.hist + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
+      cl_hist(hv, stage, f0, n, round, prefix, hr);
+      cluster_sync_all();
+      int d, nd;
+      cl_resolve<kCl>(&cs, round, need, &d, &nd);
+      prefix = round == 0 ? (uint32_t)d : (prefix << (round == 1 ? 11 : 10)) | (uint32_t)d;
+      need = nd;
     }
-    int tot_eq;
-    const int eq_incl = block_inclusive_scan(c.y, scan, &tot_eq);
-    const int eqb_q = eq_before + eq_incl - c.y;
-    const int contrib = c.x + (mode == 2 ? 0 : max(0, min(c.y, need_eq - eqb_q)));
-    int tot_c;
-    block_inclusive_scan(contrib, scan, &tot_c);
-    out_before += tot_c;
-    eq_before += tot_eq;
+    T = prefix;
+    need_eq = need;
   }
-  // each warp owns a contiguous stretch of the unit: count it, then write it
-  // in order with ballots; one block-wide exchange places the warps
-  constexpr int kWarps = kSelThreads / 32;
-  __shared__ int s_wgt[kWarps], s_weq[kWarps], s_wout[kWarps], s_weqb[kWarps];
+
+  // per-warp counts over contiguous stretches of the share, then the CTA's
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int chunk = (us.hi[ui] - us.lo[ui] + kWarps - 1) / kWarps;
-  const int lo = min(us.hi[ui], us.lo[ui] + w * chunk), hi = min(us.hi[ui], lo + chunk);
+  const int chunk = (n + kClWarps - 1) / kClWarps;
+  const int lo = min(n, w * chunk), hi = min(n, lo + chunk);
   int gtw = 0, eqw = 0;
   if (mode == 2) {
     gtw = lane == 0 ? hi - lo : 0;
-  } else {
+  } else if (mode == 1) {
     for (int i = lo + lane; i < hi; i += 32) {
-      uint32_t u;
-      int j;
-      unit_entry(v, sp, us, ui, stage, i, &u, &j);
+      const uint32_t u = (uint32_t)(share_entry(hv, stage, f0, n, i) >> 32);
       gtw += u > T;
       eqw += u == T;
     }
@@ -341,93 +327,65 @@ __device__ void unit_write(const SegView& v, const SelParams& sp, const UnitSmem
     gtw += __shfl_xor_sync(0xffffffffu, gtw, o);
     eqw += __shfl_xor_sync(0xffffffffu, eqw, o);
   }
-  if (lane == 0) { s_wgt[w] = gtw; s_weq[w] = eqw; }
+  if (lane == 0) { cs.wgt[w] = gtw; cs.weq[w] = eqw; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int ob = out_before, eb = eq_before;
-    for (int q = 0; q < kWarps; ++q) {
-      s_wout[q] = ob;
-      s_weqb[q] = eb;
-      ob += s_wgt[q] + (mode == 2 ? 0 : max(0, min(s_weq[q], need_eq - eb)));
-      eb += s_weq[q];
-    }
+    int g = 0, e = 0;
+    for (int q = 0; q < kClWarps; ++q) { g += cs.wgt[q]; e += cs.weq[q]; }
+    cs.cta_gt = g;
+    cs.cta_eq = e;
   }
-  __syncthreads();
-  int written = s_wout[w], eq_seen = s_weqb[w];
-  const unsigned lt = (1u << lane) - 1u;
-  for (int i0 = lo; i0 < hi; i0 += 32) {
-    const int i = i0 + lane;
-    uint32_t u = 0u;
-    int j = 0;
-    const bool in = i < hi;
-    if (in) unit_entry(v, sp, us, ui, stage, i, &u, &j);
-    const bool is_gt = in && (mode == 2 || u > T);
-    const bool is_eq = in && mode != 2 && u == T;
-    const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
-    const bool f = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need_eq);
-    const unsigned fb = __ballot_sync(0xffffffffu, f);
-    if (f) {
-      const int r = written + __popc(fb & lt);
-      if (r < n_take) out[sp.r_lo + r] = j;
-      else record_status(status, kStatusSelectMismatch);
-    }
-    written += __popc(fb);
-    eq_seen += __popc(eqb);
-  }
-  __syncthreads();
-}
+  cluster_sync_all();
 
-// The whole selection in one cooperative launch.  Each CTA owns up to
-// kMaxUnits units (sub-ranges of one head's key ranges).  Phases, separated
-// by grid barriers: three radix histogram rounds (each CTA resolves the
-// previous round's digit of its own heads from the global histogram), the
-// per-unit counts above and at the threshold, and the ordered write.
-__global__ void __launch_bounds__(kSelThreads)
-kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int n_units, uint32_t* __restrict__ hist,
-                  int2* __restrict__ pcnt, int32_t* __restrict__ idx, int* status) {
-  __shared__ uint32_t sh[kHist1];
-  __shared__ uint64_t stage[kStage];
-  __shared__ FindSmem fs;
-  __shared__ UnitSmem us;
-  __shared__ volatile int s_abort;
-  uint32_t* bar = hist + kHistBins;   // head 0's state word: the barrier counter
-  const int per_head = sp.nparts * kSplit;
+  // keys taken by the lower-ranked CTAs of the head: all above T and, of
+  // the ties, as many as were still needed in key order
   if (threadIdx.x == 0) {
-    s_abort = 0;
-    int n = 0;
-    for (int u = blockIdx.x; u < n_units && n < kMaxUnits; u += gridDim.x, ++n) {
-      const int seg = u / per_head, blk = u % per_head;
-      const int part = blk / kSplit, sub = blk % kSplit;
-      int64_t first;
-      const int plen = range_len(v, sp, seg, part, &first);
-      us.seg[n] = seg;
-      us.blk[n] = blk;
-      us.first[n] = first;
-      us.lo[n] = (int)((int64_t)plen * sub / kSplit);
-      us.hi[n] = (int)((int64_t)plen * (sub + 1) / kSplit);
-      us.prefix[n] = 0;
+    int ob = 0, eb = 0;
+    for (int r = 0; r < rank; ++r) {
+      const int g = (int)ld_dsmem_u32(dsmem_addr(&cs.cta_gt, (uint32_t)r));
+      const int e = (int)ld_dsmem_u32(dsmem_addr(&cs.cta_eq, (uint32_t)r));
+      ob += g + (mode == 2 ? 0 : max(0, min(e, need_eq - eb)));
+      eb += e;
     }
-    us.n = n;
-    us.staged = 0;
+    for (int q = 0; q < kClWarps; ++q) {
+      cs.wout[q] = ob;
+      cs.weqb[q] = eb;
+      ob += cs.wgt[q] + (mode == 2 ? 0 : max(0, min(cs.weq[q], need_eq - eb)));
+      eb += cs.weq[q];
+    }
   }
   __syncthreads();
-  const int nu = us.n;
-  for (int ui = 0; ui < nu; ++ui) unit_hist(v, sp, us, ui, 0, stage, sh, hist);
-  if (threadIdx.x == 0 && nu > 0) us.staged = min(us.hi[0] - us.lo[0], kStage);
-  for (int round = 1; round <= 3; ++round) {
-    if (!grid_barrier(bar, (uint32_t)round, &s_abort, status)) return;
-    for (int ui = 0; ui < nu; ++ui) {
-      unit_resolve(sp, us, ui, round - 1, hist, &fs);
-      if (round < 3 && us.mode[ui] == 1) unit_hist(v, sp, us, ui, round, stage, sh, hist);
+
+  const int n_take = mode == 0 ? 0 : mode == 2 ? E : n_sel;
+  int32_t* out = idx + (size_t)b * sp.T + sp.off[h];
+  if (rank == 0) {
+    for (int jj = threadIdx.x; jj < sp.r_lo; jj += kClThreads) out[jj] = jj;
+    for (int jj = sp.r_hi + threadIdx.x; jj < sp.S; jj += kClThreads) out[sp.r_lo + n_take + (jj - sp.r_hi)] = jj;
+  }
+  if (mode != 0) {
+    int written = cs.wout[w], eq_seen = cs.weqb[w];
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i0 = lo; i0 < hi; i0 += 32) {
+      const int i = i0 + lane;
+      const bool in = i < hi;
+      const uint64_t e = in ? share_entry(hv, stage, f0, n, i) : 0ull;
+      const uint32_t u = (uint32_t)(e >> 32);
+      const bool is_gt = in && (mode == 2 || u > T);
+      const bool is_eq = in && mode != 2 && u == T;
+      const unsigned eqb = __ballot_sync(0xffffffffu, is_eq);
+      const bool f = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need_eq);
+      const unsigned fb = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        const int r = written + __popc(fb & lt);
+        if (r < n_take) out[sp.r_lo + r] = (int32_t)(uint32_t)e;
+        else record_status(status, kStatusSelectMismatch);
+      }
+      written += __popc(fb);
+      eq_seen += __popc(eqb);
     }
   }
-  // us.prefix is now the threshold T and us.need the ties at T still needed
-  for (int ui = 0; ui < nu; ++ui) {
-    const int2 c = unit_count(v, sp, us, ui, stage, fs.scan);
-    if (threadIdx.x == 0) pcnt[(size_t)us.seg[ui] * per_head + us.blk[ui]] = c;
-  }
-  if (!grid_barrier(bar, 4u, &s_abort, status)) return;
-  for (int ui = 0; ui < nu; ++ui) unit_write(v, sp, us, ui, stage, pcnt, idx, fs.scan, status);
+  // no CTA leaves while another may still read its shared memory
+  cluster_sync_all();
 }
 
 // Gather retained rows: one 16-byte vector per lane, D/8 lanes per row.
@@ -473,24 +431,34 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
                           int32_t* idx, cudaStream_t st) {
   SegView v{mode, scores, cand, cand_cnt, cap};
   const int BH = B * sel.H_kv;
-  cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)BH * kHistPerSeg * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return e;
-  int n_units = sel.nparts * kSplit * BH;
-  static int occ[64] = {0};
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (occ[dev] == 0 &&
-      (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[dev], kvc_select_kernel, kSelThreads, 0)) != cudaSuccess)
+  cudaError_t e = cudaSuccess;
+  (void)hist;
+  (void)pcnt;
+  const int np = mode == 0 ? 1 : sel.nparts;
+  const size_t smem = (size_t)kStageC * sizeof(uint64_t) + (size_t)(np + 1) * sizeof(int);
+  if (smem > 200 * 1024) return cudaErrorInvalidConfiguration;
+  // the widest cluster that still gives every head its own CTAs in one wave
+  int cl = kMaxCl;
+  while (cl > 1 && (int64_t)BH * cl > num_sms()) cl >>= 1;
+  auto kern = cl == 8 ? kvc_select_kernel<8> : cl == 4 ? kvc_select_kernel<4> : cl == 2 ? kvc_select_kernel<2>
+                                                                                       : kvc_select_kernel<1>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
     return e;
-  const int grid = std::min(n_units, std::max(occ[dev], 1) * num_sms());
-  if ((int64_t)grid * kMaxUnits < n_units) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(BH * cl));
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int* status = status_word_ptr();
-  void* args[] = {&v, const_cast<SelParams*>(&sel), &n_units, &hist, &pcnt, &idx, &status};
-  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kvc_select_kernel), dim3(grid), dim3(kSelThreads), args,
-                                  0, st);
+  if ((e = cudaLaunchKernelEx(&cfg, kern, v, sel, idx, status)) != cudaSuccess) return e;
   note_launches(1);
-  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
