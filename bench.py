@@ -45,7 +45,13 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override the workload's S (smaller profiling captures); 0 keeps it")
     return ap.parse_args()
+
+
+def config_of(args):
+    return get_config(args.config, **({"S": args.seq_len} if args.seq_len > 0 else {}))
 
 
 def workload_desc(cfg):
@@ -158,7 +164,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    cfg = get_config(args.config)
+    cfg = config_of(args)
     S_s = min(cfg.S, 8192)
     budget_total = 150.0
     inp = make_layer_inputs(cfg.with_(S=S_s, C=min(cfg.C, S_s)), 0)
@@ -223,7 +229,7 @@ def main():
     import attention_score_kv_gb300.kvc as K
     from synth import get_config, make_layer_inputs
 
-    cfg = get_config(args.config)
+    cfg = config_of(args)
     NL = args.layers
     layers = []
     for l in range(NL):
@@ -285,7 +291,7 @@ def main():
     alg = {
         "pass1": kbytes + qbytes,
         "pass2_pool": kbytes + qbytes,
-        "select_topk": 5 * 8 * ncand + 4 * cfg.B * Tmean,
+        "select_topk": 8 * ncand + 4 * cfg.B * Tmean,
         "gather": cfg.B * Tmean * (4 * cfg.D * 2 + 4),
     }
     names = K.STAGE_NAMES
@@ -299,7 +305,7 @@ def main():
         try:
             tj = json.load(open(tfile))
             ent = tj.get(args.config, {}).get(names[dom])
-            if ent and ent.get("source_digest") == _source_digest():
+            if ent and ent.get("source_digest") == _source_digest(names[dom]):
                 traffic = ent["bytes_per_launch"]
         except (ValueError, KeyError):
             traffic = None
@@ -390,13 +396,22 @@ def main():
         dist.destroy_process_group()
 
 
-def _source_digest():
+# Sources behind each stage's kernels: a profiled traffic figure is only
+# reported while these files are unchanged since the capture.
+_STAGE_SOURCES = {
+    "pass1": ["kvc_pass1_tc.cu", "kvc_scan_common.cuh", "kvc_tc.cuh", "kvc_device.cuh", "kvc_internal.cuh"],
+    "pass2_pool": ["kvc_pass2_tc.cu", "kvc_scan_common.cuh", "kvc_tc.cuh", "kvc_device.cuh", "kvc_internal.cuh"],
+    "select_topk": ["kvc_select.cu", "kvc_device.cuh", "kvc_internal.cuh"],
+    "gather": ["kvc_select.cu", "kvc_device.cuh", "kvc_internal.cuh"],
+}
+
+
+def _source_digest(stage):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_score_kv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in _STAGE_SOURCES[stage]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
