@@ -51,6 +51,7 @@ def parse():
 
 
 def config_of(args):
+    from synth import get_config
     return get_config(args.config, **({"S": args.seq_len} if args.seq_len > 0 else {}))
 
 
