@@ -46,15 +46,16 @@ __device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int p
 
 // One thread-block cluster per (b, KV head).  The head's entries are cut
 // into kCl contiguous shares, one per CTA, and each share is copied once
-// into that CTA's shared memory (up to kStageC entries; the rest, if any, is
+// into that CTA's shared memory (up to stage_cap entries; the rest, if any, is
 // re-read from global memory in every round).  The radix rounds, the counts
 // and the ordered write then run on chip: per-CTA histograms are summed by
 // reading the other CTAs' shared memory, and hardware cluster barriers
 // separate the phases, so no CTA waits on anything outside its cluster.
-constexpr int kMaxCl = 8;               // CTAs per head at most (portable cluster size)
+constexpr int kMaxCl = 16;              // CTAs per head at most (a non-portable cluster size)
 constexpr int kClThreads = 512;
 constexpr int kClWarps = kClThreads / 32;
-constexpr int kStageC = 16384;          // entries per CTA kept in shared memory
+constexpr int kStageC = 16384;          // entries per CTA kept in shared memory (clusters of <= 8)
+constexpr int kStageC16 = 8192;         // ... in clusters of 16, two CTAs per SM
 constexpr int kCopyBatch = 8;
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -103,6 +104,7 @@ struct HeadView {
   int seg;
   const int* pref;
   int nparts;
+  int stage_cap;   // entries of the share held in shared memory
 };
 
 __device__ __forceinline__ uint64_t head_entry(const HeadView& hv, int f) {
@@ -123,7 +125,7 @@ __device__ __forceinline__ uint64_t head_entry(const HeadView& hv, int f) {
 
 // Entry f0 + i of this CTA's share (n entries).
 __device__ __forceinline__ uint64_t share_entry(const HeadView& hv, const uint64_t* stage, int f0, int n, int i) {
-  return (n <= kStageC || i < kStageC) ? stage[i] : head_entry(hv, f0 + i);
+  return (n <= hv.stage_cap || i < hv.stage_cap) ? stage[i] : head_entry(hv, f0 + i);
 }
 
 __device__ __forceinline__ int radix_bin(uint32_t u, int round, uint32_t prefix) {
@@ -207,11 +209,12 @@ __device__ void cl_resolve(ClSmem* cs, int round, int need, int* digit, int* nee
 }
 
 template <int kCl>
-__global__ void __launch_bounds__(kClThreads, 1)
-kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int32_t* __restrict__ idx, int* status) {
+__global__ void __launch_bounds__(kClThreads, kCl == 16 ? 2 : 1)
+kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap, int32_t* __restrict__ idx,
+                  int* status) {
   extern __shared__ __align__(16) uint8_t cl_dyn[];
   uint64_t* stage = reinterpret_cast<uint64_t*>(cl_dyn);
-  int* pref = reinterpret_cast<int*>(cl_dyn + (size_t)kStageC * sizeof(uint64_t));
+  int* pref = reinterpret_cast<int*>(cl_dyn + (size_t)stage_cap * sizeof(uint64_t));
   __shared__ ClSmem cs;
   const int seg = blockIdx.x / kCl;
   const int rank = (int)cluster_rank();
@@ -242,14 +245,14 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int32_t* __re
     E = carry;
   }
   __syncthreads();
-  HeadView hv{&v, &sp, seg, pref, nparts};
+  HeadView hv{&v, &sp, seg, pref, nparts, stage_cap};
   const int f0 = (int)((int64_t)E * rank / kCl), f1 = (int)((int64_t)E * (rank + 1) / kCl);
   const int n = f1 - f0;
   const int mode = n_sel <= 0 ? 0 : n_sel >= E ? 2 : 1;
 
   // copy this CTA's share into shared memory, list by list
   if (mode != 0) {
-    const int ns = min(n, kStageC);
+    const int ns = min(n, stage_cap);
     if (v.mode == 0) {
       for (int i0 = 0; i0 < ns; i0 += kCopyBatch * kClThreads) {
         uint64_t t[kCopyBatch];
@@ -435,13 +438,53 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   (void)hist;
   (void)pcnt;
   const int np = mode == 0 ? 1 : sel.nparts;
-  const size_t smem = (size_t)kStageC * sizeof(uint64_t) + (size_t)(np + 1) * sizeof(int);
-  if (smem > 200 * 1024) return cudaErrorInvalidConfiguration;
-  // the widest cluster that still gives every head its own CTAs in one wave
-  int cl = kMaxCl;
+  auto smem_for = [np](int cap) { return (size_t)cap * sizeof(uint64_t) + (size_t)(np + 1) * sizeof(int); };
+  if (smem_for(kStageC) > 200 * 1024) return cudaErrorInvalidConfiguration;
+  // the widest cluster that still gives every head its own CTAs in one wave;
+  // 16 (two CTAs per SM, smaller shared-memory shares) only where the device
+  // co-schedules a cluster of 16 for every head at once
+  // (short heads keep clusters of 8: their shares are small already)
+  int cl = sel.S >= 65536 ? kMaxCl : 8;
   while (cl > 1 && (int64_t)BH * cl > num_sms()) cl >>= 1;
-  auto kern = cl == 8 ? kvc_select_kernel<8> : cl == 4 ? kvc_select_kernel<4> : cl == 2 ? kvc_select_kernel<2>
-                                                                                       : kvc_select_kernel<1>;
+  auto pick = [](int c) {
+    return c == 16 ? kvc_select_kernel<16> : c == 8 ? kvc_select_kernel<8> : c == 4 ? kvc_select_kernel<4>
+           : c == 2 ? kvc_select_kernel<2> : kvc_select_kernel<1>;
+  };
+  static int s_ncl16[64] = {0};   // per device: clusters of 16 resident at once + 1 (0: not asked yet)
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cl == 16 && s_ncl16[dev] > 0) cl = s_ncl16[dev] - 1 >= BH ? 16 : 8;
+  if (cl == 16 && s_ncl16[dev] == 0) {
+    auto k16 = pick(16);
+    int nclusters = 0;
+    bool ok16 = cudaFuncSetAttribute(k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+                cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_for(kStageC16)) ==
+                    cudaSuccess;
+    if (ok16) {
+      cudaLaunchConfig_t q{};
+      q.gridDim = dim3((unsigned)(BH * 16));
+      q.blockDim = dim3(kClThreads);
+      q.dynamicSmemBytes = smem_for(kStageC16);
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 16;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      ok16 = cudaOccupancyMaxActiveClusters(&nclusters, k16, &q) == cudaSuccess;
+    }
+    if (!ok16) {
+      (void)cudaGetLastError();
+      nclusters = 0;
+    }
+    s_ncl16[dev] = nclusters + 1;
+    if (nclusters < BH) cl = 8;
+  }
+  const int stage_cap = cl == 16 ? kStageC16 : kStageC;
+  const size_t smem = smem_for(stage_cap);
+  auto kern = pick(cl);
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
     return e;
   cudaLaunchConfig_t cfg{};
@@ -457,7 +500,7 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int* status = status_word_ptr();
-  if ((e = cudaLaunchKernelEx(&cfg, kern, v, sel, idx, status)) != cudaSuccess) return e;
+  if ((e = cudaLaunchKernelEx(&cfg, kern, v, sel, stage_cap, idx, status)) != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
 }
