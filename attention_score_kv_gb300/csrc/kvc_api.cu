@@ -139,15 +139,12 @@ bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int
     L->plan = ScanPlan{0, 0, 0, 0};
     L->slots = max_slots(BH);
   }
-  const int parts = max_parts(BH);
   L->gwp = (gw + 15) / 16 * 16;
   L->cap = std::max(K_l_max, 0) + b_s;
   size_t o = 0;
   L->off_bias = o;     o = align256(o + (size_t)BH * L->gwp * sizeof(float));
   L->off_part_m = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
   L->off_part_z = o;   o = align256(o + (size_t)L->slots * L->gwp * sizeof(float));
-  L->off_hist = o;     o = align256(o + (size_t)BH * kHistPerSeg * sizeof(uint32_t));
-  L->off_pcnt = o;     o = align256(o + (size_t)BH * parts * kSelectSplit * sizeof(int2));
   L->off_cand_cnt = o; o = align256(o + (size_t)L->slots * sizeof(int));
   L->off_cand = o;     o = align256(o + (size_t)L->slots * (size_t)L->cap * sizeof(uint64_t));
   L->total = o;
@@ -302,10 +299,10 @@ int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* 
     return rc;
   WsLayout L;
   if (!layout_ws(B, H_q, H_kv, D, W, b_s, 0, pool_k, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
-  if ((rc = check_ws(ws, ws_bytes, L.off_bias + (size_t)B * H_kv * L.gwp * sizeof(float)))) return rc;
   SelParams sp{};
   sp.S = S;
   sp.H_kv = H_kv;
+  if ((rc = check_ws(ws, ws_bytes, L.off_bias + (size_t)B * H_kv * L.gwp * sizeof(float)))) return rc;
   Pass2Out out{scores, nullptr, nullptr, 0};
   float* bias = reinterpret_cast<float*>(static_cast<char*>(ws) + L.off_bias);
   return launch_status(launch_pass2(reinterpret_cast<const __nv_bfloat16*>(q_win),
@@ -323,15 +320,10 @@ int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* 
   if ((rc = check_ptr(scores, 4, "scores")) || (rc = check_ptr(idx, 4, "idx"))) return rc;
   SelParams sp;
   if ((rc = make_sel(S, H_kv, K_l, sink, recent, &sp, nullptr))) return rc;
-  WsLayout L;
-  if (!layout_ws(B, H_kv, H_kv, 64, 1, kTile, 0, 1, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
-  const int BH = B * H_kv;
-  sp.nparts = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(2 * (int64_t)num_sms(), BH), max_parts(BH)));
-  if ((rc = check_ws(ws, ws_bytes, L.off_pcnt + (size_t)BH * max_parts(BH) * kSelectSplit * sizeof(int2)))) return rc;
-  char* w = static_cast<char*>(ws);
-  return launch_status(launch_select(0, scores, nullptr, nullptr, 0, B, sp, reinterpret_cast<uint32_t*>(w + L.off_hist),
-                                     reinterpret_cast<int2*>(w + L.off_pcnt), idx,
-                                     reinterpret_cast<cudaStream_t>(stream)),
+  (void)ws;
+  (void)ws_bytes;
+  sp.nparts = 1;
+  return launch_status(launch_select(0, scores, nullptr, nullptr, 0, B, sp, idx, reinterpret_cast<cudaStream_t>(stream)),
                        "selection launch");
 }
 
@@ -400,8 +392,7 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
                           "pass 2 launch")))
     return rc;
   if (ev) cudaEventRecord(ev[2], st);
-  if ((rc = launch_status(launch_select(1, nullptr, cand, cnt, L.cap, B, sp, reinterpret_cast<uint32_t*>(w + L.off_hist),
-                                        reinterpret_cast<int2*>(w + L.off_pcnt), pos_out, st),
+  if ((rc = launch_status(launch_select(1, nullptr, cand, cnt, L.cap, B, sp, pos_out, st),
                           "selection launch")))
     return rc;
   if (ev) cudaEventRecord(ev[3], st);

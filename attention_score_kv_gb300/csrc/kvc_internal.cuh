@@ -16,24 +16,9 @@ constexpr int kMaxGWP = 256;        // G*W rounded up to 16
 constexpr int kMaxPool = 15;        // widest average pool
 constexpr int kMaxSeg = 8;          // KV heads one scan CTA may touch
 constexpr int kMinKeysPerCta = 1024;
-constexpr int kSelectSplit = 4;     // selection CTAs per key range
 constexpr int kHist1 = 2048;        // radix digits: bits 31..21, 20..10, 9..0 of the score
 constexpr int kHist2 = 2048;
 constexpr int kHist3 = 1024;
-constexpr int kHistBins = kHist1 + kHist2 + kHist3;
-constexpr int kHistPerSeg = kHistBins + 8;   // + SelState
-
-// Per-head selection state, zeroed before the histogram rounds; the last CTA
-// of each round resolves that round's digit here for the later kernels.
-struct SelState {
-  uint32_t done[3];   // CTAs finished per round
-  int total;          // candidate keys of the head
-  int mode;           // 0: keep none, 1: rank, 2: keep every candidate
-  uint32_t prefix;    // score-bit digits found so far (after round 3: the threshold T)
-  int need;           // keys still needed among those sharing the prefix
-  int pad;
-};
-static_assert(sizeof(SelState) == 32, "SelState must fit the 8 words after the histograms");
 
 // device status word codes
 constexpr int kStatusOk = 0;
@@ -60,8 +45,6 @@ struct WsLayout {
   int cap;         // candidate capacity per slot (K_l_max + b_s)
   size_t off_bias;                 // float  [BH][gwp]    pass-2 per-row bias
   size_t off_part_m, off_part_z;   // float  [slots][gwp]
-  size_t off_hist;                 // uint32 [BH][kHistPerSeg]
-  size_t off_pcnt;                 // int2   [BH][plan.nparts * kSelectSplit]
   size_t off_cand_cnt;             // int    [slots]
   size_t off_cand;                 // uint64 [slots][cap]
   size_t total;
@@ -111,7 +94,7 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
                          cudaStream_t st);
 // selection over dense scores (mode 0) or candidate lists (mode 1)
 cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt, int cap, int B,
-                          const SelParams& sel, uint32_t* hist, int2* pcnt, int32_t* idx, cudaStream_t st);
+                          const SelParams& sel, int32_t* idx, cudaStream_t st);
 cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* idx, int B, int H_kv,
                           int S, int D, int64_t T, const int64_t* off_host, __nv_bfloat16* k_out,
                           __nv_bfloat16* v_out, int32_t* pos_out, cudaStream_t st);

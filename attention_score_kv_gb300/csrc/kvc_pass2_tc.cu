@@ -296,66 +296,6 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         const int j = t0 + krow;
         const bool need_mask = (t0 + kTile - 1 > A.S - A.W);
         float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-#if KVC_TMEM_PIPE
-        // next batch's tensor-memory loads in flight while this batch is summed
-        float va[64], vb[64];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (i < nch) tc::tmem_ld16(taddr + i * 16, va + 16 * i);
-        tc::tmem_wait_ld();
-        tc::reg_fence(va, 64);
-#pragma unroll
-        for (int bt = 0; bt < 4; ++bt) {
-          if (bt < nbt) {
-            float(&cur)[64] = (bt & 1) ? vb : va;
-            float(&nxt)[64] = (bt & 1) ? va : vb;
-            if (bt + 1 < nbt) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (4 * (bt + 1) + i < nch) tc::tmem_ld16(taddr + (4 * (bt + 1) + i) * 16, nxt + 16 * i);
-            } else {
-              tc::fence_before_sync();
-              __syncwarp();
-              if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[g]));
-            }
-            if (!need_mask) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if (4 * bt + i < nch) {
-#pragma unroll
-                  for (int q = 0; q < 16; q += 8) {
-                    const float* w = cur + 16 * i + q;
-                    a0.x += ex2(w[0] * c2);
-                    a0.y += ex2(w[1] * c2);
-                    a1.x += ex2(w[2] * c2);
-                    a1.y += ex2(w[3] * c2);
-                    a2.x += ex2(w[4] * c2);
-                    a2.y += ex2(w[5] * c2);
-                    a3.x += ex2(w[6] * c2);
-                    a3.y += ex2(w[7] * c2);
-                  }
-                }
-              }
-            } else {
-              const int dj = j - (A.S - A.W);
-              for (int i = 0; i < 4; ++i) {
-                if (4 * bt + i < nch) {
-                  int wi = ((4 * bt + i) * 16) % A.W;
-                  for (int q = 0; q < 16; ++q) {
-                    const float e = ex2(cur[16 * i + q] * c2);
-                    a0.x += wi >= dj ? e : 0.f;
-                    if (++wi == A.W) wi = 0;
-                  }
-                }
-              }
-            }
-            if (bt + 1 < nbt) {
-              tc::tmem_wait_ld();
-              tc::reg_fence(nxt, 64);
-            }
-          }
-        }
-#else
 #pragma unroll 1
         for (int bt = 0; bt < nbt; ++bt) {
           float v[64];
@@ -376,16 +316,6 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
 #pragma unroll
                 for (int q = 0; q < 16; q += 8) {
                   const float* w = v + 16 * i + q;
-#if KVC_EXP_SCALAR
-                  a0.x += ex2(w[0] * c2);
-                  a0.y += ex2(w[1] * c2);
-                  a1.x += ex2(w[2] * c2);
-                  a1.y += ex2(w[3] * c2);
-                  a2.x += ex2(w[4] * c2);
-                  a2.y += ex2(w[5] * c2);
-                  a3.x += ex2(w[6] * c2);
-                  a3.y += ex2(w[7] * c2);
-#else
                   const float2 x0 = __fmul2_rn(make_float2(w[0], w[1]), cc);
                   const float2 x1 = __fmul2_rn(make_float2(w[2], w[3]), cc);
                   const float2 x2 = __fmul2_rn(make_float2(w[4], w[5]), cc);
@@ -394,7 +324,6 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
                   a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
                   a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
                   a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
-#endif
                 }
               }
             }
@@ -416,7 +345,6 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
             }
           }
         }
-#endif
         float r = (a0.x + a0.y) + (a1.x + a1.y) + ((a2.x + a2.y) + (a3.x + a3.y));
         if (j < 0 || j >= A.S) r = 0.f;
         const int slot = tcount % kRing;

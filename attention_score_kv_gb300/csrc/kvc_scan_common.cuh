@@ -39,10 +39,6 @@ constexpr uint32_t kAccStride = 256;          // TMEM columns per accumulator bu
 constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSegs = 8;
-#ifndef KVC_PREFETCH_TILES
-#define KVC_PREFETCH_TILES 0
-#endif
-constexpr int kPrefetchTiles = KVC_PREFETCH_TILES;   // L2 prefetch distance of the key tiles
 
 struct ScanArgs {
   int B, H_q, H_kv, S, W, gw, gwp16, n_mb, nq, P, maxseg, pool_k, cap;
@@ -166,14 +162,7 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
       tc::tma_load_3d(sQ + kh * q_half, qmap, smem_u32(&bars->qfull), kh * 64, qrow, 0);
     const int start = sg.a - hw;
     const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
-    // key tiles run kPrefetchTiles ahead into L2, so the shared-memory ring
-    // only has to cover L2 latency
-    for (int t = 0; t < min(ntiles, kPrefetchTiles); ++t)
-      for (int kh = 0; kh < NKH; ++kh) tc::tma_prefetch_l2_3d(kmap, kh * 64, start + t * kTile, sg.bh);
     for (int t = 0; t < ntiles; ++t) {
-      if (t + kPrefetchTiles < ntiles)
-        for (int kh = 0; kh < NKH; ++kh)
-          tc::tma_prefetch_l2_3d(kmap, kh * 64, start + (t + kPrefetchTiles) * kTile, sg.bh);
       if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, A.status)) return;
       const uint32_t dst = sK + stage * kTileBytes;
       tc::mbar_arrive_expect_tx(smem_u32(&bars->full[stage]), kTileBytes);

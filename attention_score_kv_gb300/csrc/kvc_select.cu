@@ -430,13 +430,10 @@ kvc_gather_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
 }  // namespace
 
 cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt,
-                          int cap, int B, const SelParams& sel, uint32_t* hist, int2* pcnt,
-                          int32_t* idx, cudaStream_t st) {
+                          int cap, int B, const SelParams& sel, int32_t* idx, cudaStream_t st) {
   SegView v{mode, scores, cand, cand_cnt, cap};
   const int BH = B * sel.H_kv;
   cudaError_t e = cudaSuccess;
-  (void)hist;
-  (void)pcnt;
   const int np = mode == 0 ? 1 : sel.nparts;
   auto smem_for = [np](int cap) { return (size_t)cap * sizeof(uint64_t) + (size_t)(np + 1) * sizeof(int); };
   if (smem_for(kStageC) > 200 * 1024) return cudaErrorInvalidConfiguration;
