@@ -74,6 +74,25 @@ int max_parts(int BH);                              // S-independent bound on pl
 bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int pool_k, int S,
                WsLayout* L);                        // S < 0: the S-independent upper bound
 
+// Launch `kernel` so that it may start while the previous grid on the stream
+// finishes (programmatic stream serialization); the kernel calls
+// grid_dep_wait() before it touches anything that grid produces.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // --------------------------------------------------------- kernel launchers
 // pass 1: per-slot partial normalisers (log2-domain max, Z relative to it)
 cudaError_t launch_pass1(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S, int D,

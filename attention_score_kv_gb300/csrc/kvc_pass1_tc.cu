@@ -113,6 +113,9 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
+  // everything above overlaps the previous grid; its outputs are read below
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -240,6 +243,8 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
 // m, Z (natural-log units) of every window row from the pass-1 slots.
 __global__ void kvc_pass1_combine_kernel(const __grid_constant__ ScanArgs A, float* __restrict__ m,
                                          float* __restrict__ Z) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int bh = blockIdx.x;
   const int b = bh / A.H_kv, h = bh % A.H_kv, G = A.H_q / A.H_kv;
   for (int r = threadIdx.x; r < A.gw; r += blockDim.x) {
@@ -255,7 +260,7 @@ cudaError_t launch(Kern kernel, int grid, size_t smem, cudaStream_t st, const Sc
                    const CUtensorMap& km) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, smem, st>>>(A, qm, km);
+  if ((e = launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, st, A, qm, km)) != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
 }
@@ -286,7 +291,8 @@ cudaError_t launch_pass1_combine(const float* part_m, const float* part_z, int B
   ScanArgs A = base_args(pl, B, H_q, H_kv, S, 64, W);
   A.pm_in = part_m;
   A.pz_in = part_z;
-  kvc_pass1_combine_kernel<<<B * H_kv, 256, 0, st>>>(A, m, Z);
+  const cudaError_t e = launch_pdl(kvc_pass1_combine_kernel, dim3(B * H_kv), dim3(256), 0, st, A, m, Z);
+  if (e != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
 }

@@ -258,6 +258,9 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
+  // everything above overlaps the previous grid; its outputs are read below
+  grid_dep_wait();
+  grid_dep_launch();
 
   const int hw = (A.pool_k - 1) / 2;
   Seg segs[kMaxSegs];
@@ -455,6 +458,8 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
 // One warp per window row: the lanes merge the row's pass-1 slots in
 // parallel, then a butterfly merges the lanes.
 __global__ void kvc_lse_bias_kernel(const __grid_constant__ ScanArgs A, float* __restrict__ bias) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
   const int r = blockIdx.x * (blockDim.x >> 5) + warp;
@@ -493,7 +498,7 @@ cudaError_t launch(Kern kernel, int grid, size_t smem, cudaStream_t st, const Sc
                    const CUtensorMap& qm, const CUtensorMap& km) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, smem, st>>>(A, sp, qm, km);
+  if ((e = launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, st, A, sp, qm, km)) != cudaSuccess) return e;
   note_launches(1);
   return cudaGetLastError();
 }
@@ -517,9 +522,8 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
   A.cand = out.cand;
   A.cand_cnt = out.cand_cnt;
   A.cap = out.cap;
-  kvc_lse_bias_kernel<<<dim3((A.gwp16 + 7) / 8, B * H_kv), 256, 0, st>>>(A, bias_ws);
+  cudaError_t e = launch_pdl(kvc_lse_bias_kernel, dim3((A.gwp16 + 7) / 8, B * H_kv), dim3(256), 0, st, A, bias_ws);
   note_launches(1);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap qm, km;
   if (!make_map(&qm, q, D, (uint64_t)B * H_q * W, 1, A.nq) || !make_map(&km, k, D, S, (uint64_t)B * H_kv, kTile))

@@ -223,6 +223,8 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
   const int nparts = v.mode == 0 ? 1 : sp.nparts;
 
   for (int i = threadIdx.x; i < kHist1 + kHist2 + kHist3; i += kClThreads) cs.hist[i] = 0u;
+  grid_dep_wait();   // the scores or candidate lists come from the previous grid
+  grid_dep_launch();
   // list lengths and their exclusive prefix (mode 1), else the dense range
   int E;
   if (v.mode == 0) {
@@ -398,6 +400,8 @@ kvc_gather_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
               const int32_t* idx, const __grid_constant__ SelParams sp, int B,
               __nv_bfloat16* __restrict__ k_out, __nv_bfloat16* __restrict__ v_out, int32_t* pos_out,
               int* status) {
+  grid_dep_wait();   // the positions come from the previous grid
+  grid_dep_launch();
   constexpr int LPR = D / 8;             // lanes per row
   constexpr int RPW = 32 / LPR;          // rows per warp step
   const int lane = threadIdx.x & 31;
@@ -489,13 +493,15 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   cfg.blockDim = dim3(kClThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   int* status = status_word_ptr();
   if ((e = cudaLaunchKernelEx(&cfg, kern, v, sel, stage_cap, idx, status)) != cudaSuccess) return e;
   note_launches(1);
@@ -515,11 +521,15 @@ cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const 
   const int rows_per_block = (256 / 32) * (32 / (D / 8));
   int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
   if (blocks > 4 * 1024) blocks = 4 * 1024;
+  cudaError_t e;
   if (D == 64)
-    kvc_gather_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
+    e = launch_pdl(kvc_gather_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, st, k, v, idx, sp, B, k_out, v_out,
+                   pos_out, status_word_ptr());
   else
-    kvc_gather_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(k, v, idx, sp, B, k_out, v_out, pos_out, status_word_ptr());
+    e = launch_pdl(kvc_gather_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, st, k, v, idx, sp, B, k_out, v_out,
+                   pos_out, status_word_ptr());
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
