@@ -307,7 +307,7 @@ int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* 
   float* bias = reinterpret_cast<float*>(static_cast<char*>(ws) + L.off_bias);
   return launch_status(launch_pass2(reinterpret_cast<const __nv_bfloat16*>(q_win),
                                     reinterpret_cast<const __nv_bfloat16*>(k), m, Z, nullptr, nullptr, bias, B, H_q,
-                                    H_kv, S, D, W, pool_k, L.plan, L.gwp, &sp, out,
+                                    H_kv, S, D, W, pool_k, L.plan, L.gwp, &sp, out, false,
                                     reinterpret_cast<cudaStream_t>(stream)),
                        "pass 2 launch");
 }
@@ -388,7 +388,7 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
   Pass2Out out{nullptr, cand, cnt, L.cap};
   float* bias = reinterpret_cast<float*>(w + L.off_bias);
   if ((rc = launch_status(launch_pass2(q, kk, nullptr, nullptr, pm, pz, bias, B, H_q, H_kv, S, D, W, pool_k, L.plan,
-                                       L.gwp, &sp, out, st),
+                                       L.gwp, &sp, out, true, st),
                           "pass 2 launch")))
     return rc;
   if (ev) cudaEventRecord(ev[2], st);

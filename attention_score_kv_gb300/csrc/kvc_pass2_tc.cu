@@ -258,8 +258,10 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  // everything above overlaps the previous grid; its outputs are read below
-  grid_dep_wait();
+  // Everything above overlaps the previous grid.  Its outputs (the row
+  // biases) are read below; when the keys and queries are known to be ready,
+  // the TMA warp starts loading them at once.
+  if (!(A.inputs_ready && warp == 0)) grid_dep_wait();
   grid_dep_launch();
 
   const int hw = (A.pool_k - 1) / 2;
@@ -508,11 +510,12 @@ cudaError_t launch(Kern kernel, int grid, size_t smem, cudaStream_t st, const Sc
 cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const float* m, const float* Z,
                          const float* part_m, const float* part_z, float* bias_ws, int B, int H_q, int H_kv, int S,
                          int D, int W, int pool_k, const ScanPlan& pl, int gwp, const SelParams* sel, Pass2Out out,
-                         cudaStream_t st) {
+                         bool inputs_ready, cudaStream_t st) {
   (void)gwp;
   ScanArgs A = base_args(pl, B, H_q, H_kv, S, D, W);
   A.nq = A.gwp16;
   A.pool_k = pool_k;
+  A.inputs_ready = inputs_ready ? 1 : 0;
   A.m_in = m;
   A.z_in = Z;
   A.pm_in = part_m;

@@ -42,6 +42,7 @@ constexpr int kMaxSegs = 8;
 
 struct ScanArgs {
   int B, H_q, H_kv, S, W, gw, gwp16, n_mb, nq, P, maxseg, pool_k, cap;
+  int inputs_ready;          // pass 2: keys and queries were complete before the previous grid ran
   int64_t L;
   float c2;                  // log2(e) / sqrt(D)
   float* part_m;             // pass 1 out: [P*maxseg][gwp16] (log2 units)
