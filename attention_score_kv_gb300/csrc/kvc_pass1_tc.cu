@@ -45,12 +45,12 @@ __device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, uint32_t adrain, co
   const uint32_t idesc = tc::idesc_bf16(128, 128);
   const uint32_t tq = tmem + kQCol;
   uint32_t stage = 0, phase = 0, qphase = 0, u = 0;
-  for (int s = 0; s < nseg; ++s) {
-    const Seg sg = segs[s];
+  for (int si = 0; si < nseg; ++si) {
+    const Seg sg = segs[si];
     if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) return;
     qphase ^= 1;
     // the previous segment's MMAs must be done reading the old queries
-    if (s > 0 && !wait_bar(adrain, (uint32_t)(s - 1) & 1u, abort_flag, A.status)) return;
+    if (si > 0 && !wait_bar(adrain, (uint32_t)(si - 1) & 1u, abort_flag, A.status)) return;
     tc::fence_after_sync();
     for (int mb = 0; mb < A.n_mb; ++mb)
 #pragma unroll
@@ -77,7 +77,7 @@ __device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, uint32_t adrain, co
       tc::mma_commit(smem_u32(&bars->empty[stage]));
       if (++stage == kStages) { stage = 0; phase ^= 1; }
     }
-    if (s + 1 < nseg) tc::mma_commit(adrain);
+    if (si + 1 < nseg) tc::mma_commit(adrain);
   }
 }
 
@@ -143,12 +143,13 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
     const int nseg = cta_segments(A, blockIdx.x, segs);
     uint32_t tcount = 0;
     bool ok = true;
-    for (int s = 0; s < nseg && ok; ++s) {
-      const Seg sg = segs[s];
+    for (int si = 0; si < nseg && ok; ++si) {
+      const Seg sg = segs[si];
       float mrun = -INFINITY;
       float2 z2 = make_float2(0.f, 0.f);
       const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
-      for (int t = 0; t < ntiles; ++t, ++tcount) {
+      for (int ti = 0; ti < ntiles; ++ti, ++tcount) {
+        const int t = p1_tile_order(ti, ntiles);
         const uint32_t u = NMB == 2 ? 2 * tcount + mb : tcount;   // this warp's sub-tile
         const uint32_t buf = p1_buf(u);
         if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), p1_parity(u), &s_abort, A.status)) { ok = false; break; }

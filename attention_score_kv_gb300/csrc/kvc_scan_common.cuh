@@ -82,6 +82,14 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, vol
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Pass-1 tile order within a segment: the leading third of the keys comes
+// last, so pass 2, which starts there, finds those keys still in L2.  Each
+// stretch is read in ascending order.
+__device__ __forceinline__ int p1_tile_order(int i, int ntiles) {
+  const int lead = ntiles / 3;
+  return i < ntiles - lead ? lead + i : i - (ntiles - lead);
+}
+
 // Segments of CTA c, in key order.
 __device__ __forceinline__ int cta_segments(const ScanArgs& A, int c, Seg* out) {
   const int64_t total = (int64_t)A.B * A.H_kv * A.S;
@@ -150,9 +158,9 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
   const int nseg = cta_segments(A, blockIdx.x, segs);
   const int G = A.H_q / A.H_kv;
   uint32_t stage = 0, phase = 0, qphase = 0;
-  for (int s = 0; s < nseg; ++s) {
-    const Seg sg = segs[s];
-    if (s > 0) {
+  for (int si = 0; si < nseg; ++si) {
+    const Seg sg = segs[si];
+    if (si > 0) {
       if (!wait_bar(smem_u32(&bars->qempty), qphase, abort_flag, A.status)) return;
       qphase ^= 1;
     }
@@ -163,7 +171,8 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
       tc::tma_load_3d(sQ + kh * q_half, qmap, smem_u32(&bars->qfull), kh * 64, qrow, 0);
     const int start = sg.a - hw;
     const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
-    for (int t = 0; t < ntiles; ++t) {
+    for (int ti = 0; ti < ntiles; ++ti) {
+      const int t = PASS == 1 ? p1_tile_order(ti, ntiles) : ti;
       if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, A.status)) return;
       const uint32_t dst = sK + stage * kTileBytes;
       tc::mbar_arrive_expect_tx(smem_u32(&bars->full[stage]), kTileBytes);
@@ -172,58 +181,6 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
                         sg.bh);
       if (++stage == NST) { stage = 0; phase ^= 1; }
     }
-  }
-}
-
-// MMA issuer (one thread).  Pass 1: A = window queries (M = 128 per block),
-// B = key tile (N = 128).  Pass 2: A = key tile (M = 128), B = window queries
-// (N = G*W rounded to 16).  Both operands K-major bf16 in 128-byte swizzle.
-template <int D, int PASS>
-__device__ void mma_issuer(const ScanArgs& A, PipeBars* bars, uint32_t sQ, uint32_t sK, uint32_t tmem,
-                           volatile int* abort_flag) {
-  constexpr int NKH = D / 64;
-  constexpr int KSTEPS = D / 16;
-  constexpr uint32_t kTileBytes = kTile * 128 * NKH;
-  const uint32_t q_half = (uint32_t)A.nq * 128;
-  const int hw = PASS == 2 ? (A.pool_k - 1) / 2 : 0;
-  Seg segs[kMaxSegs];
-  const int nseg = cta_segments(A, blockIdx.x, segs);
-  uint32_t stage = 0, phase = 0, qphase = 0, buf = 0, tphase = 0;
-  const uint32_t idesc = PASS == 1 ? tc::idesc_bf16(128, 128) : tc::idesc_bf16(128, A.gwp16);
-  for (int s = 0; s < nseg; ++s) {
-    const Seg sg = segs[s];
-    if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) return;
-    qphase ^= 1;
-    const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
-    for (int t = 0; t < ntiles; ++t) {
-      if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status)) return;
-      if (!wait_bar(smem_u32(&bars->tempty[buf]), tphase ^ 1, abort_flag, A.status)) return;
-      tc::fence_after_sync();
-      const uint32_t kb = sK + stage * kTileBytes;
-      const uint32_t dacc = tmem + buf * kAccStride;
-      if (PASS == 1) {
-        for (int mb = 0; mb < A.n_mb; ++mb) {
-#pragma unroll
-          for (int ks = 0; ks < KSTEPS; ++ks) {
-            const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
-            const uint32_t qoff = (ks >> 2) * q_half + mb * (128 * 128) + (ks & 3) * 32;
-            tc::mma_bf16(dacc + mb * 128, tc::desc_sw128(sQ + qoff), tc::desc_sw128(kb + koff), idesc, ks > 0);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-          const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
-          const uint32_t qoff = (ks >> 2) * q_half + (ks & 3) * 32;
-          tc::mma_bf16(dacc, tc::desc_sw128(kb + koff), tc::desc_sw128(sQ + qoff), idesc, ks > 0);
-        }
-      }
-      tc::mma_commit(smem_u32(&bars->empty[stage]));
-      tc::mma_commit(smem_u32(&bars->tfull[buf]));
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
-      if (++buf == 2) { buf = 0; tphase ^= 1; }
-    }
-    tc::mma_commit(smem_u32(&bars->qempty));
   }
 }
 
