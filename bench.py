@@ -55,6 +55,29 @@ def config_of(args):
     return get_config(args.config, **({"S": args.seq_len} if args.seq_len > 0 else {}))
 
 
+# ---- replica bookkeeping (no CUDA needed; the multi-process CPU tests use it)
+def replica_layer_ids(rank, n_local, n_layers):
+    """Layers rank `rank` compresses: n_local distinct ones, disjoint across
+    ranks while world * n_local <= n_layers."""
+    return [(rank * n_local + l) % n_layers for l in range(n_local)]
+
+
+def max_over_ranks(value, world, device=None):
+    """The slowest rank's elapsed time (all_reduce MAX), or value at N=1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_step, steps, ms):
+    """Units processed by all ranks per second over the slowest rank's time."""
+    return world * units_per_step * steps / (ms / 1e3)
+
+
 def workload_desc(cfg):
     kl = f"K_l={cfg.K_l}" if not cfg.inverse_stability else f"K_l~1/s, {cfg.budget_frac:.0%} of S*H_kv"
     return (f"{cfg.name}: N={cfg.N} B={cfg.B} H_q={cfg.H_q} H_kv={cfg.H_kv} D={cfg.D} S={cfg.S} C={cfg.C} "
@@ -233,8 +256,7 @@ def main():
     cfg = config_of(args)
     NL = args.layers
     layers = []
-    for l in range(NL):
-        layer_id = (rank * NL + l) % cfg.N
+    for layer_id in replica_layer_ids(rank, NL, cfg.N):
         inp = make_layer_inputs(cfg, layer_id, device=dev)
         kl = budgets(cfg, K, layer_id)
         k_out, v_out, pos, off = K.retained_outputs(cfg.B, cfg.H_kv, cfg.S, cfg.D, kl, device=dev)
@@ -281,15 +303,13 @@ def main():
     torch.cuda.synchronize(dev)
     stage_ms, calls, launches = K.kvc_profile_end()
     launches = launches * args.steps // max(calls, 1)
+    ms = max_over_ranks(ms, world, dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     K.kvc_check_status(stream)
 
     units_per_step = cfg.B * cfg.H_kv * cfg.S
-    value = world * units_per_step * args.steps / (ms / 1e3)
+    value = job_throughput(world, units_per_step, args.steps, ms)
 
     # ---- roofline of the dominant kernel (algorithmic bytes per launch)
     hbm_peak, _, peak_kind = load_peaks()
@@ -365,12 +385,9 @@ def main():
         a1.record(stream)
         torch.cuda.synchronize(dev)
         ems = a0.elapsed_time(a1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems, world, dev)
         L0 = layers[0]
-        e2e = {"value": world * units_per_step * args.e2e_steps / (ems / 1e3), "unit": UNIT,
+        e2e = {"value": job_throughput(world, units_per_step, args.e2e_steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": (L0["q"].numel() + L0["k"].numel() + L0["v"].numel()) * 2,
                "d2h_bytes_per_step": (L0["k_out"].numel() + L0["v_out"].numel()) * 2 + L0["pos"].numel() * 4,
                "ms_per_step": ems / args.e2e_steps}
