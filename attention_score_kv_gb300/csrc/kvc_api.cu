@@ -312,6 +312,23 @@ int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k, const float* 
                        "pass 2 launch");
 }
 
+int kvc_score_rawdot_int8(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, int H_kv, int S, int D,
+                          int W, float* scores, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  int rc;
+  if ((rc = check_shapes(B, H_q, H_kv, S, D, W))) return rc;
+  if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(scores, 4, "scores")))
+    return rc;
+  const size_t BH = (size_t)B * H_kv;
+  const size_t off_scale = align256(BH * (size_t)D);
+  if ((rc = check_ws(ws, ws_bytes, off_scale + BH * sizeof(float)))) return rc;
+  char* w = static_cast<char*>(ws);
+  return launch_status(launch_rawdot_int8(reinterpret_cast<const __nv_bfloat16*>(q_win),
+                                          reinterpret_cast<const __nv_bfloat16*>(k), B, H_q, H_kv, S, D, W,
+                                          reinterpret_cast<int8_t*>(w), reinterpret_cast<float*>(w + off_scale),
+                                          scores, reinterpret_cast<cudaStream_t>(stream)),
+                       "INT8 raw-product scorer launch");
+}
+
 int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* K_l, int sink, int recent,
                     int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream) {
   int rc;

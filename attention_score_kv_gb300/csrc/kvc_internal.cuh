@@ -111,6 +111,10 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
                          const float* part_m, const float* part_z, float* bias_ws, int B, int H_q, int H_kv, int S,
                          int D, int W, int pool_k, const ScanPlan& pl, int gwp, const SelParams* sel, Pass2Out out,
                          bool inputs_ready, cudaStream_t st);
+// single-pass raw inner-product scores with INT8 keys: query codes and
+// scales of every head into qcode [BH][D] / qscale [BH], then dense scores
+cudaError_t launch_rawdot_int8(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S,
+                               int D, int W, int8_t* qcode, float* qscale, float* scores, cudaStream_t st);
 // selection over dense scores (mode 0) or candidate lists (mode 1)
 cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt, int cap, int B,
                           const SelParams& sel, int32_t* idx, cudaStream_t st);

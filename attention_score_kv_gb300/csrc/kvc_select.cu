@@ -2,8 +2,11 @@
 //
 // Selection keeps, per (b, KV head), the mandatory set R_mand = [0, sink) u
 // [S - recent, S) and the n_sel best other keys by (score desc, index asc),
-// listed in ascending position.  Scores are >= 0, so their fp32 bit patterns
-// order like the values; a three-round radix select over those bits (11, 11
+// listed in ascending position.  Scores become 32-bit keys that order like
+// the values (the fused scorer's scores are >= 0 and keep their fp32 bits;
+// dense scores of either sign are mapped by flipping the sign bit of
+// positive values and all bits of negative ones); a three-round radix select
+// over those bits (11, 11
 // and 10 bits, each round a histogram of the keys that share the digits found
 // so far) finds the n_sel-th score T and how many keys scoring exactly T are
 // still needed.  Ties at T are taken in ascending index order, resolved with
@@ -111,7 +114,8 @@ __device__ __forceinline__ uint64_t head_entry(const HeadView& hv, int f) {
   if (hv.v->mode == 0) {
     const int j = hv.sp->r_lo + f;
     uint32_t bits = __float_as_uint(hv.v->scores[(size_t)hv.seg * hv.sp->S + j]);
-    bits = (bits == 0x80000000u) ? 0u : bits;
+    bits = (bits == 0x80000000u) ? 0u : bits;                      // -0 ranks as +0
+    bits = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);    // order-preserving for either sign
     return ((uint64_t)bits << 32) | (uint32_t)j;
   }
   int lo = 0, hi = hv.nparts - 1;   // last part whose list starts at or before f

@@ -62,6 +62,7 @@ _SIGS = {
     "kvc_score_pass1": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "kvc_score_pass1_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_score_pass2_pool": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "kvc_score_rawdot_int8": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvc_select_topk": (_I, [_P, _I, _I, _I, _I32P, _I, _I, _P, _P, _SZ, _P]),
     "kvc_gather": (_I, [_P, _P, _P, _I, _I, _I, _I, _I32P, _P, _P, _P, _P]),
     "kvc_compress_layer": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I32P, _I, _I, _I, _I,
@@ -141,6 +142,11 @@ def kvc_score_pass2_pool(q_win, k, m, Z, B, H_q, H_kv, S, D, W, b_s, pool_k, sco
     _check(_lib.kvc_score_pass2_pool(_ptr(q_win), _ptr(k), _ptr(m), _ptr(Z), B, H_q, H_kv, S, D, W, b_s,
                                      pool_k, _ptr(scores), _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
                                      _stream(stream)))
+
+
+def kvc_score_rawdot_int8(q_win, k, B, H_q, H_kv, S, D, W, scores, ws, ws_bytes=None, stream=None):
+    _check(_lib.kvc_score_rawdot_int8(_ptr(q_win), _ptr(k), B, H_q, H_kv, S, D, W, _ptr(scores), _ptr(ws),
+                                      ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
 
 
 def kvc_select_topk(scores, B, H_kv, S, K_l, sink, recent, idx, ws, ws_bytes=None, stream=None):

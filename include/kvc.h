@@ -126,9 +126,31 @@ int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k,
                          kvc_stream_t stream);
 
 /*
+ * Single-pass raw inner-product scores with INT8 keys (HillInfer,
+ * "Algorithmic Simplification" and "Streaming Execution and Asymmetric
+ * Precision"): no exponentials and no 1/sqrt(D), one read of K.
+ *   q_win  [B, H_q, W, D] bf16; the scoring query of KV head h is the
+ *          float32 sum of its group's G*W window rows, in row order
+ *   k      [B, H_kv, S, D] bf16
+ *   scores [B, H_kv, S] fp32 out (any sign):
+ *          float32(float32(dot_j) * scale_q) * scale_k, where each row (the
+ *          scoring query, each key) is cast to symmetric INT8 with
+ *          code = rint(x * (127 / max|x|)) in [-127, 127], scale = max|x| /
+ *          127, and dot_j is the exact integer product of the codes.
+ *   ws     >= B*H_kv*(D + 4) + 256 bytes, 256-byte aligned (the query codes
+ *          and scales); kvc_workspace_size(...) bytes always suffice.
+ * Rank the scores with kvc_select_topk and fetch the full-precision rows
+ * with kvc_gather.  Errors as for the other calls.
+ */
+int kvc_score_rawdot_int8(const kvc_bf16* q_win, const kvc_bf16* k, int B,
+                          int H_q, int H_kv, int S, int D, int W,
+                          float* scores, void* ws, size_t ws_bytes,
+                          kvc_stream_t stream);
+
+/*
  * Per-head selection (TideKV Fig. 3): keep R_mand and the top
  * (K_l[h] - |R_mand|) other keys by (score descending, index ascending).
- *   scores [B, H_kv, S] fp32 (>= 0)
+ *   scores [B, H_kv, S] fp32, finite, any sign (-0 ranks as +0)
  *   K_l    HOST [H_kv]; K_l[h] >= |R_mand|.  A head with K_l[h] >= S keeps
  *          every key.
  *   idx    out, int32 positions, ascending within each head.  Head h of

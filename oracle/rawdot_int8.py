@@ -39,7 +39,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["summed_query", "quantize_int8", "raw_scores_exact", "raw_scores_int8", "int8_error_bound"]
+__all__ = ["summed_query", "quantize_int8", "raw_scores_exact", "raw_scores_int8", "raw_scores_int8_rows",
+           "int8_error_bound"]
 
 _F127 = np.float32(127.0)
 
@@ -84,7 +85,8 @@ def raw_scores_exact(q_grp, k) -> np.ndarray:
 
 
 def raw_scores_int8(q_grp, k) -> np.ndarray:
-    """float32 INT8 raw scores of every key of one head (see header)."""
+    """float32 INT8 raw scores of every key of one head (see header), one key
+    at a time."""
     qc, sq = quantize_int8(summed_query(q_grp))
     kk = _f32(k)
     out = np.empty(kk.shape[0], dtype=np.float32)
@@ -93,6 +95,23 @@ def raw_scores_int8(q_grp, k) -> np.ndarray:
         dot = int(np.dot(qc.astype(np.int64), kc.astype(np.int64)))
         out[j] = np.float32(np.float32(np.float32(dot) * sq) * sk)
     return out
+
+
+def raw_scores_int8_rows(q_grp, k) -> np.ndarray:
+    """raw_scores_int8 for many keys at once: the same float32 operations,
+    element by element, on whole arrays (for full-size heads)."""
+    qc, sq = quantize_int8(summed_query(q_grp))
+    kk = _f32(k)
+    amax = np.max(np.abs(kk), axis=1).astype(np.float32)
+    nz = amax > 0
+    inv = np.zeros_like(amax)
+    inv[nz] = (_F127 / amax[nz]).astype(np.float32)
+    codes = np.clip(np.rint((kk * inv[:, None]).astype(np.float32)), -127, 127).astype(np.int64)
+    codes[~nz] = 0
+    sk = np.zeros_like(amax)
+    sk[nz] = (amax[nz] / _F127).astype(np.float32)
+    dot = codes @ qc.astype(np.int64)
+    return ((dot.astype(np.float32) * sq).astype(np.float32) * sk).astype(np.float32)
 
 
 def int8_error_bound(q_grp, k) -> np.ndarray:

@@ -88,3 +88,13 @@ def test_selection_handles_negative_scores():
     assert idx.tolist() == [0, 3, 5, 7]
     idx = O.select_topk(s, 5, 1, 1)      # ... then the tie at -1.0 goes to index 1
     assert idx.tolist() == [0, 1, 3, 5, 7]
+
+
+def test_row_batched_scores_equal_the_per_key_ones():
+    rng = np.random.default_rng(9)
+    q = (rng.standard_normal((6, 64)) * 2).astype(np.float32)
+    k = (rng.standard_normal((300, 64)) * rng.uniform(0.001, 100, (300, 1))).astype(np.float32)
+    k[11] = 0.0
+    a = R.raw_scores_int8(q, k)
+    b = R.raw_scores_int8_rows(q, k)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
