@@ -13,17 +13,14 @@
 // reproducible bit for bit.
 //
 // Kernel 1 builds the query codes of every head; kernel 2 streams the keys
-// once: D/8 lanes per key row, one 16-byte load per lane, the row maximum
-// by shuffles, the dot product by dp4a.
+// once: D/32 lanes per key row, the row maximum by shuffles, the dot product
+// by dp4a.
 #include <algorithm>
 
-#include "kvc_device.cuh"
-#include "kvc_internal.cuh"
+#include "kvc_scan_common.cuh"
 
 namespace kvc {
 namespace {
-
-constexpr int kRowsPerThreadStep = 2;   // independent rows in flight per lane
 
 __device__ __forceinline__ int code8(float x, float inv) {
   const int c = __float2int_rn(__fmul_rn(x, inv));
@@ -54,60 +51,134 @@ __global__ void kvc_rawdot_query_kernel(const __nv_bfloat16* __restrict__ q, int
   if (d == 0) qscale[bh] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
 }
 
+// Key rows stream through a shared-memory ring filled by bulk copies (one
+// producer thread), so the bytes in flight do not depend on the consumers'
+// registers.  Each CTA owns a contiguous range of rows; a stage holds
+// 32 KB of rows.  Eight consumer warps take their rows in two passes, four
+// lanes per row (two at D = 64), 32 elements per lane.  Lane (row sub, c)
+// reads 16-byte chunk (4i + c + sub) mod (D/8) of its row at step i: the
+// eight rows of a warp then fall on distinct shared-memory bank groups.
+constexpr int kRingStages = 3;          // 3 x 32 KB: two CTAs per SM
+constexpr int kRingPasses = 2;          // row passes of each consumer warp per stage
+constexpr int kConsumerWarps = 8;
+constexpr int kRawThreads = 32 * (1 + kConsumerWarps);
 template <int D>
-__global__ void __launch_bounds__(256)
-kvc_rawdot_score_kernel(const __nv_bfloat16* __restrict__ k, int64_t rows, int S, const int8_t* __restrict__ qcode,
-                        const float* __restrict__ qscale, float* __restrict__ scores) {
+__host__ __device__ constexpr int ring_rows() { return kConsumerWarps * (32 / (D / 32)) * kRingPasses; }   // 32 KB of rows
+
+template <int D>
+__global__ void __launch_bounds__(kRawThreads)
+kvc_rawdot_score_kernel(const __nv_bfloat16* __restrict__ k, int64_t rows, int64_t per_cta, int S,
+                        const int8_t* __restrict__ qcode, const float* __restrict__ qscale, float* __restrict__ scores,
+                        int* status) {
+  constexpr int ROWB = D * 2;              // bytes per key row
+  constexpr int NCH = ROWB / 16;           // 16-byte chunks per row
+  constexpr int LPR = D / 32;              // lanes per row
+  constexpr int NLD = NCH / LPR;           // chunks per lane
+  constexpr int kRingRows = ring_rows<D>();
+  constexpr uint32_t kStageBytes = kRingRows * ROWB;
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kRingStages], empty[kRingStages];
+  __shared__ volatile int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRingStages; ++i) {
+      tc::mbar_init(smem_u32(&full[i]), 1);
+      tc::mbar_init(smem_u32(&empty[i]), kConsumerWarps);
+    }
+    s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
   grid_dep_wait();   // the query codes come from the previous grid
   grid_dep_launch();
-  constexpr int LPR = D / 8;             // lanes per key row
-  constexpr int RPW = 32 / LPR;          // rows per warp step
-  const int lane = threadIdx.x & 31;
-  const int sub = lane / LPR, cl = lane % LPR;
-  const unsigned group_mask = (LPR == 32) ? 0xffffffffu : (((1u << LPR) - 1u) << (sub * LPR));
-  const int64_t warp_g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t stride = nwarps * RPW;
-  for (int64_t r0 = warp_g * RPW + sub; r0 - sub < rows; r0 += kRowsPerThreadStep * stride) {
-    uint4 raw[kRowsPerThreadStep];
-#pragma unroll
-    for (int u = 0; u < kRowsPerThreadStep; ++u) {
-      const int64_t r = r0 + u * stride;
-      raw[u] = r < rows ? __ldg(reinterpret_cast<const uint4*>(k + (size_t)r * D) + cl) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kRowsPerThreadStep; ++u) {
-      const int64_t r = r0 + u * stride;
-      const int bh = (int)((r < rows ? r : 0) / S);
-      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
-      float x[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(p2[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
+  const int64_t r_a = (int64_t)blockIdx.x * per_cta;
+  const int64_t r_b = min(rows, r_a + per_cta);
+  const int nchunks = r_a < r_b ? (int)((r_b - r_a + kRingRows - 1) / kRingRows) : 0;
+  const uint32_t base = smem_u32(ring);
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0;
+      for (int t = 0; t < nchunks; ++t) {
+        if (!scan::wait_bar(smem_u32(&empty[st]), ph ^ 1u, &s_abort, status)) break;
+        const int64_t r = r_a + (int64_t)t * kRingRows;
+        const uint32_t bytes = (uint32_t)(min((int64_t)kRingRows, r_b - r) * ROWB);
+        tc::mbar_arrive_expect_tx(smem_u32(&full[st]), bytes);
+        tc::bulk_g2s(base + st * kStageBytes, k + (size_t)r * D, bytes, smem_u32(&full[st]));
+        if (++st == kRingStages) { st = 0; ph ^= 1u; }
       }
-      float a = 0.f;
+    }
+    return;
+  }
+  const int w = warp - 1;
+  const int sub = lane / LPR, cl = lane % LPR;
+  const unsigned group_mask = ((1u << LPR) - 1u) << (sub * LPR);
+  constexpr int RPW = 32 / LPR;            // rows per warp per pass
+  uint32_t st = 0, ph = 0;
+  for (int t = 0; t < nchunks; ++t) {
+    if (!scan::wait_bar_warp(smem_u32(&full[st]), ph, &s_abort, status)) break;
+    const int64_t r0 = r_a + (int64_t)t * kRingRows;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+    for (int pass = 0; pass < kRingPasses; ++pass) {
+      const int rr = (pass * kConsumerWarps + w) * RPW + sub;   // row within the stage
+      const int64_t r = r0 + rr;
+      const bool valid = r < r_b;
+      const uint32_t rowaddr = base + st * kStageBytes + rr * ROWB;
+      uint4 raw[NLD];
+      int chs[NLD];
+#pragma unroll
+      for (int i = 0; i < NLD; ++i) {
+        chs[i] = (i * LPR + cl + sub) % NCH;
+        raw[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (valid)
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                       : "=r"(raw[i].x), "=r"(raw[i].y), "=r"(raw[i].z), "=r"(raw[i].w)
+                       : "r"(rowaddr + chs[i] * 16));
+      }
+      const int bh = (int)((valid ? r : r0) / S);
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < NLD; ++i) {
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(p2[e]);
+          a0 = fmaxf(a0, fabsf(f.x));
+          a1 = fmaxf(a1, fabsf(f.y));
+        }
+      }
+      float a = fmaxf(a0, a1);
 #pragma unroll
       for (int o = LPR / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(group_mask, a, o));
+      // |x| <= a and inv = fl(127/a), so |x * inv| < 127.5: rint stays in
+      // [-127, 127] without a clamp
       const float inv = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
-      int c[8];
+      int dot = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = a > 0.f ? code8(x[i], inv) : 0;
-      const int kp0 = (c[0] & 0xff) | ((c[1] & 0xff) << 8) | ((c[2] & 0xff) << 16) | ((c[3] & 0xff) << 24);
-      const int kp1 = (c[4] & 0xff) | ((c[5] & 0xff) << 8) | ((c[6] & 0xff) << 16) | ((c[7] & 0xff) << 24);
-      const int2 qp = *reinterpret_cast<const int2*>(qcode + (size_t)bh * D + cl * 8);
-      int dot = __dp4a(kp0, qp.x, 0);
-      dot = __dp4a(kp1, qp.y, dot);
+      for (int i = 0; i < NLD; ++i) {
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+        int c[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(p2[e]);
+          c[2 * e] = __float2int_rn(__fmul_rn(f.x, inv));
+          c[2 * e + 1] = __float2int_rn(__fmul_rn(f.y, inv));
+        }
+        const int kp0 = (c[0] & 0xff) | ((c[1] & 0xff) << 8) | ((c[2] & 0xff) << 16) | (c[3] << 24);
+        const int kp1 = (c[4] & 0xff) | ((c[5] & 0xff) << 8) | ((c[6] & 0xff) << 16) | (c[7] << 24);
+        const int2 qp = *reinterpret_cast<const int2*>(qcode + (size_t)bh * D + chs[i] * 8);
+        dot = __dp4a(kp0, qp.x, dot);
+        dot = __dp4a(kp1, qp.y, dot);
+      }
 #pragma unroll
       for (int o = LPR / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(group_mask, dot, o);
-      if (cl == 0 && r < rows) {
+      if (cl == 0 && valid) {
         const float sk = a > 0.f ? __fdiv_rn(a, 127.f) : 0.f;
         scores[r] = __fmul_rn(__fmul_rn((float)dot, qscale[bh]), sk);
       }
     }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(smem_u32(&empty[st]));
+    if (++st == kRingStages) { st = 0; ph ^= 1u; }
   }
 }
 
@@ -120,15 +191,23 @@ cudaError_t launch_rawdot_int8(const __nv_bfloat16* q, const __nv_bfloat16* k, i
   note_launches(1);
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)BH * S;
-  const int rows_per_block = (256 / 32) * (32 / (D / 8)) * kRowsPerThreadStep;
-  int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-  blocks = std::min<int64_t>(std::max<int64_t>(blocks, 1), (int64_t)num_sms() * 16);
-  if (D == 64)
-    e = launch_pdl(kvc_rawdot_score_kernel<64>, dim3((unsigned)blocks), dim3(256), 0, st, k, rows, S, qcode, qscale,
-                   scores);
-  else
-    e = launch_pdl(kvc_rawdot_score_kernel<128>, dim3((unsigned)blocks), dim3(256), 0, st, k, rows, S, qcode, qscale,
-                   scores);
+  const int ctas = std::max(1, num_sms() * 2);
+  const int64_t per_cta = (rows + ctas - 1) / ctas;
+  const size_t smem = (size_t)kRingStages * (D == 64 ? ring_rows<64>() : ring_rows<128>()) * D * 2;
+  const int grid = (int)((rows + per_cta - 1) / per_cta);
+  if (D == 64) {
+    if ((e = cudaFuncSetAttribute(kvc_rawdot_score_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess)
+      return e;
+    e = launch_pdl(kvc_rawdot_score_kernel<64>, dim3(grid), dim3(kRawThreads), smem, st, k, rows, per_cta, S, qcode,
+                   qscale, scores, status_word_ptr());
+  } else {
+    if ((e = cudaFuncSetAttribute(kvc_rawdot_score_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess)
+      return e;
+    e = launch_pdl(kvc_rawdot_score_kernel<128>, dim3(grid), dim3(kRawThreads), smem, st, k, rows, per_cta, S, qcode,
+                   qscale, scores, status_word_ptr());
+  }
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

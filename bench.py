@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["two_pass", "rawdot_int8"], default="two_pass",
+                    help="two_pass: the layer compress (default, the headline); rawdot_int8: the single-pass "
+                         "INT8 raw inner-product scorer, then the same selection and gather")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's S (smaller profiling captures); 0 keeps it")
     return ap.parse_args()
@@ -232,10 +235,108 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_rawdot(args):
+    """One step = INT8 raw-product scores, selection, gather over one layer
+    (1 GPU).  Prints one JSON line like the headline's, with the scorer as
+    the dominant kernel of the roofline."""
+    import torch
+    from attention_score_kv_gb300 import build as _b
+    _b.build()
+    import attention_score_kv_gb300.kvc as K
+    from synth import make_layer_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cfg = config_of(args)
+    layers = []
+    for layer_id in replica_layer_ids(0, args.layers, cfg.N):
+        inp = make_layer_inputs(cfg, layer_id, device=dev)
+        kl = budgets(cfg, K, layer_id)
+        k_out, v_out, pos, off = K.retained_outputs(cfg.B, cfg.H_kv, cfg.S, cfg.D, kl, device=dev)
+        layers.append(dict(q=inp.q_win, k=inp.k, v=inp.v, K_l=kl, k_out=k_out, v_out=v_out, pos=pos, T=off[-1]))
+    ws = K.workspace(cfg.B, cfg.H_q, cfg.H_kv, cfg.D, cfg.W, cfg.b_s, max(max(L["K_l"]) for L in layers),
+                     cfg.pool_k, device=dev)
+    scores = torch.empty((cfg.B, cfg.H_kv, cfg.S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_prof = min(args.steps, 50)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
+
+    def step(i, marks=False):
+        L = layers[i % len(layers)]
+        ev = evs[i] if marks else None
+        if marks:
+            ev[0].record(stream)
+        K.kvc_score_rawdot_int8(L["q"], L["k"], cfg.B, cfg.H_q, cfg.H_kv, cfg.S, cfg.D, cfg.W, scores, ws,
+                                stream=stream)
+        if marks:
+            ev[1].record(stream)
+        K.kvc_select_topk(scores, cfg.B, cfg.H_kv, cfg.S, L["K_l"], cfg.sink, cfg.recent, L["pos"], ws,
+                          stream=stream)
+        if marks:
+            ev[2].record(stream)
+        K.kvc_gather(L["k"], L["v"], L["pos"], cfg.B, cfg.H_kv, cfg.S, cfg.D, L["K_l"], L["k_out"], L["v_out"],
+                     L["pos"], stream=stream)
+        if marks:
+            ev[3].record(stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    K.kvc_check_status(stream)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.15)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    stage = [0.0, 0.0, 0.0]
+    for i in range(n_prof):
+        step(i, marks=True)
+    torch.cuda.synchronize(dev)
+    for i in range(n_prof):
+        for t in range(3):
+            stage[t] += evs[i][t].elapsed_time(evs[i][t + 1])
+    K.kvc_check_status(stream)
+    stage = [x / n_prof for x in stage]
+    units = cfg.B * cfg.H_kv * cfg.S
+    Tmean = sum(L["T"] for L in layers) / len(layers)
+    kbytes = cfg.B * cfg.H_kv * cfg.S * cfg.D * 2
+    hbm_peak, _, peak_kind = load_peaks()
+    alg = [kbytes + cfg.B * cfg.H_q * cfg.W * cfg.D * 2 + 4 * units, 4 * units + 4 * cfg.B * Tmean,
+           cfg.B * Tmean * (4 * cfg.D * 2 + 4)]
+    dom = max(range(3), key=lambda t: stage[t])
+    names = ["rawdot_int8", "select_topk", "gather"]
+    achieved = alg[dom] / (stage[dom] / 1e3) / 1e9
+    path_bytes = sum(alg)
+    line = {
+        "metric": METRIC, "value": job_throughput(1, units, args.steps, ms), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 scores, bf16 rows", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "path": "rawdot_int8 (HillInfer raw q.k, INT8 keys)",
+                   "parallelism": "replicas x1",
+                   "l2": f"inputs larger than L2: {len(layers)} distinct layers cycled"},
+        "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                     "alg_bytes_per_launch": alg[dom], "ms_per_launch": stage[dom]},
+        "path_hbm_gbs": path_bytes / (ms / args.steps / 1e3) / 1e9,
+        "stage_ms_per_launch": {n: round(t, 5) for n, t in zip(names, stage)},
+        "gpu_launches": 4 * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.path == "rawdot_int8":
+        run_rawdot(args)
         return
     import torch
     import torch.distributed as dist
