@@ -461,6 +461,42 @@ int kvc_budget_inverse_stability(int H_kv, const double* s_stable, int64_t total
   return KVC_OK;
 }
 
+int kvc_overlap_coefficient(const int32_t* a, const int64_t* a_off, const int32_t* b, const int64_t* b_off,
+                            int n_pairs, float* out, kvc_stream_t stream) {
+  int rc;
+  if (n_pairs < 0) return set_error(KVC_ERR_INVALID_ARG, "n_pairs must be >= 0");
+  if (n_pairs == 0) return KVC_OK;
+  if ((rc = check_ptr(a, 4, "a")) || (rc = check_ptr(b, 4, "b")) || (rc = check_ptr(a_off, 8, "a_off")) ||
+      (rc = check_ptr(b_off, 8, "b_off")) || (rc = check_ptr(out, 4, "out")))
+    return rc;
+  if (n_pairs > (1 << 30)) return set_error(KVC_ERR_UNSUPPORTED, "n_pairs above 2^30");
+  return launch_status(launch_overlap(a, a_off, b, b_off, n_pairs, out, reinterpret_cast<cudaStream_t>(stream)),
+                       "overlap launch");
+}
+
+int kvc_head_similarity(const int32_t* idx, const int64_t* off, int n_groups, int H, float* sim,
+                        kvc_stream_t stream) {
+  int rc;
+  if (n_groups < 1 || H < 1) return set_error(KVC_ERR_INVALID_ARG, "n_groups and H must be >= 1");
+  if (H > 65535 || n_groups > 65535) return set_error(KVC_ERR_UNSUPPORTED, "n_groups and H must be <= 65535");
+  if ((rc = check_ptr(idx, 4, "idx")) || (rc = check_ptr(off, 8, "off")) || (rc = check_ptr(sim, 4, "sim")))
+    return rc;
+  return launch_status(launch_similarity(idx, off, n_groups, H, sim, reinterpret_cast<cudaStream_t>(stream)),
+                       "similarity launch");
+}
+
+int kvc_budget_inverse_stability_device(int n_layers, int H_kv, const double* s_stable, int64_t total, int lo,
+                                        int hi, int32_t* K_l_out, kvc_stream_t stream) {
+  int rc;
+  if (n_layers < 1 || H_kv < 1) return set_error(KVC_ERR_INVALID_ARG, "n_layers and H_kv must be >= 1");
+  if (H_kv > kMaxHkv) return set_error(KVC_ERR_UNSUPPORTED, "H_kv=%d above %d", H_kv, kMaxHkv);
+  if (total < 0 || lo < 0 || hi < lo) return set_error(KVC_ERR_INVALID_ARG, "need total >= 0 and 0 <= lo <= hi");
+  if ((rc = check_ptr(s_stable, 8, "s_stable")) || (rc = check_ptr(K_l_out, 4, "K_l_out"))) return rc;
+  return launch_status(launch_budget(s_stable, n_layers, H_kv, total, lo, hi, K_l_out,
+                                     reinterpret_cast<cudaStream_t>(stream)),
+                       "budget launch");
+}
+
 int kvc_profile_begin(void) {
   g_prof = true;
   g_prof_used = 0;
@@ -498,7 +534,9 @@ int kvc_check_status(kvc_stream_t stream) {
   if (v == kStatusOk) return KVC_OK;
   if (v == kStatusTimeout) return set_error(KVC_ERR_TIMEOUT, "a device wait gave up");
   return set_error(KVC_ERR_DEVICE, "kernel status %d (%s)", v,
-                   v == kStatusCandOverflow ? "candidate list overflow" : "selection count mismatch");
+                   v == kStatusCandOverflow   ? "candidate list overflow"
+                   : v == kStatusBadInput     ? "a device-resident input broke the contract"
+                                              : "selection count mismatch");
 }
 
 }  // extern "C"

@@ -25,6 +25,7 @@ constexpr int kStatusOk = 0;
 constexpr int kStatusCandOverflow = 1;
 constexpr int kStatusSelectMismatch = 2;
 constexpr int kStatusTimeout = 3;
+constexpr int kStatusBadInput = 4;      // a device-resident input broke the contract
 
 // How the flattened key space [B*H_kv][S] is cut into scan CTAs: CTA c owns
 // keys [c*L, (c+1)*L) and touches at most `maxseg` KV heads; one head is
@@ -115,6 +116,14 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
 // scales of every head into qcode [BH][D] / qscale [BH], then dense scores
 cudaError_t launch_rawdot_int8(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S,
                                int D, int W, int8_t* qcode, float* qscale, float* scores, cudaStream_t st);
+// HeteroCache measurement and allocation (overlap coefficient, head
+// similarity, inverse-stability budgets on the device)
+cudaError_t launch_overlap(const int32_t* a, const int64_t* a_off, const int32_t* b, const int64_t* b_off,
+                           int n_pairs, float* out, cudaStream_t st);
+cudaError_t launch_similarity(const int32_t* idx, const int64_t* off, int n_groups, int H, float* sim,
+                              cudaStream_t st);
+cudaError_t launch_budget(const double* s_stable, int n_layers, int H, int64_t total, int lo, int hi,
+                          int32_t* K_l, cudaStream_t st);
 // selection over dense scores (mode 0) or candidate lists (mode 1)
 cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt, int cap, int B,
                           const SelParams& sel, int32_t* idx, cudaStream_t st);

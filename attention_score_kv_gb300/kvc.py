@@ -67,6 +67,9 @@ _SIGS = {
     "kvc_gather": (_I, [_P, _P, _P, _I, _I, _I, _I, _I32P, _P, _P, _P, _P]),
     "kvc_compress_layer": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I32P, _I, _I, _I, _I,
                                 _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "kvc_overlap_coefficient": (_I, [_P, _P, _P, _P, _I, _P, _P]),
+    "kvc_head_similarity": (_I, [_P, _P, _I, _I, _P, _P]),
+    "kvc_budget_inverse_stability_device": (_I, [_I, _I, _P, _I64, _I, _I, _P, _P]),
     "kvc_retained_layout": (_I, [_I, _I, _I32P, _I64P]),
     "kvc_budget_inverse_stability": (_I, [_I, _F64P, _I64, _I, _I, _I32P]),
     "kvc_check_status": (_I, [_P]),
@@ -147,6 +150,20 @@ def kvc_score_pass2_pool(q_win, k, m, Z, B, H_q, H_kv, S, D, W, b_s, pool_k, sco
 def kvc_score_rawdot_int8(q_win, k, B, H_q, H_kv, S, D, W, scores, ws, ws_bytes=None, stream=None):
     _check(_lib.kvc_score_rawdot_int8(_ptr(q_win), _ptr(k), B, H_q, H_kv, S, D, W, _ptr(scores), _ptr(ws),
                                       ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def kvc_overlap_coefficient(a, a_off, b, b_off, n_pairs, out, stream=None):
+    _check(_lib.kvc_overlap_coefficient(_ptr(a), _ptr(a_off), _ptr(b), _ptr(b_off), n_pairs, _ptr(out),
+                                        _stream(stream)))
+
+
+def kvc_head_similarity(idx, off, n_groups, H, sim, stream=None):
+    _check(_lib.kvc_head_similarity(_ptr(idx), _ptr(off), n_groups, H, _ptr(sim), _stream(stream)))
+
+
+def kvc_budget_inverse_stability_device(n_layers, H_kv, s_stable, total, lo, hi, K_l_out, stream=None):
+    _check(_lib.kvc_budget_inverse_stability_device(n_layers, H_kv, _ptr(s_stable), total, lo, hi, _ptr(K_l_out),
+                                                    _stream(stream)))
 
 
 def kvc_select_topk(scores, B, H_kv, S, K_l, sink, recent, idx, ws, ws_bytes=None, stream=None):

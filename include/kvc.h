@@ -193,6 +193,49 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q,
                        kvc_stream_t stream);
 
 /*
+ * Overlap coefficient of index sets (HeteroCache, "Key Contributions" 1 and
+ * "Methodology", Phase 1): out[i] = |A_i n B_i| / min(|A_i|, |B_i|), fp32
+ * (|A n B| and the minimum are exact integers, divided once in float32),
+ * 0 when either set is empty.  The measure behind HeteroCache's stability
+ * score (a head's decoding top-k against its prefill set).
+ *   a, b          int32 positions; set i is a[a_off[i] .. a_off[i+1]-1], each
+ *                 set ascending and without duplicates (as kvc_select_topk
+ *                 writes them)
+ *   a_off, b_off  int64 [n_pairs + 1], device
+ *   out           fp32 [n_pairs], device
+ */
+int kvc_overlap_coefficient(const int32_t* a, const int64_t* a_off,
+                            const int32_t* b, const int64_t* b_off,
+                            int n_pairs, float* out, kvc_stream_t stream);
+
+/*
+ * HeteroCache's similarity score of every head (Phase 1): for each group g
+ * (say a batch element of one layer) of H index sets and each head i,
+ * sim[g*H + i] = max over j != i of the overlap coefficient of sets i and j
+ * (0 when H = 1).
+ *   idx  int32 positions, sets as in kvc_overlap_coefficient
+ *   off  int64 [n_groups][H + 1], device: set (g, i) is
+ *        idx[off[g][i] .. off[g][i+1]-1]
+ *   sim  fp32 [n_groups * H], device
+ */
+int kvc_head_similarity(const int32_t* idx, const int64_t* off, int n_groups,
+                        int H, float* sim, kvc_stream_t stream);
+
+/*
+ * kvc_budget_inverse_stability on the device, for n_layers layers at once
+ * (HeteroCache, Phase 2): the same float64 operations in the same order, so
+ * the budgets equal the host function's.
+ *   s_stable  fp64 [n_layers][H_kv], device, each > 0 and finite; a layer
+ *             with a bad score gets lo everywhere and the status word records
+ *             KVC_ERR_DEVICE (see kvc_check_status)
+ *   K_l_out   int32 [n_layers][H_kv], device
+ */
+int kvc_budget_inverse_stability_device(int n_layers, int H_kv,
+                                        const double* s_stable, int64_t total,
+                                        int lo, int hi, int32_t* K_l_out,
+                                        kvc_stream_t stream);
+
+/*
  * Host helper: CSR layout of one batch element's retained rows.
  * out_off HOST [H_kv + 1]: head h owns rows out_off[h] .. out_off[h+1]-1,
  * with min(K_l[h], S) rows; out_off[H_kv] is the per-batch-element stride T.
