@@ -435,6 +435,40 @@ int kvc_retained_layout(int H_kv, int S, const int32_t* K_l, int64_t* out_off) {
   return KVC_OK;
 }
 
+int kvc_append_chunk(const kvc_bf16* k_chunk, const kvc_bf16* v_chunk, int B, int H_kv, int S, int C, int D, int j,
+                     kvc_bf16* k_act, kvc_bf16* v_act, kvc_stream_t stream) {
+  int rc;
+  if (B < 1 || H_kv < 1 || S < 1 || C < 1) return set_error(KVC_ERR_INVALID_ARG, "B, H_kv, S and C must be >= 1");
+  if (D != 64 && D != 128) return set_error(KVC_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are supported", D);
+  if (j < 0 || (int64_t)j * C >= S)
+    return set_error(KVC_ERR_INVALID_ARG, "chunk %d of size %d starts beyond S=%d", j, C, S);
+  if ((rc = check_ptr(k_chunk, 16, "k_chunk")) || (rc = check_ptr(v_chunk, 16, "v_chunk")) ||
+      (rc = check_ptr(k_act, 16, "k_act")) || (rc = check_ptr(v_act, 16, "v_act")))
+    return rc;
+  return launch_status(launch_append_chunk(reinterpret_cast<const __nv_bfloat16*>(k_chunk),
+                                           reinterpret_cast<const __nv_bfloat16*>(v_chunk), B, H_kv, S, C, D, j,
+                                           reinterpret_cast<__nv_bfloat16*>(k_act),
+                                           reinterpret_cast<__nv_bfloat16*>(v_act),
+                                           reinterpret_cast<cudaStream_t>(stream)),
+                       "chunk append launch");
+}
+
+int kvc_cache_layout(int N, int B, int H_kv, int S, const int32_t* K_l, int64_t* layer_row_off) {
+  if (N < 1 || B < 1 || H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "N, B, H_kv and S must be >= 1");
+  if (!K_l || !layer_row_off) return set_error(KVC_ERR_INVALID_ARG, "K_l and layer_row_off must be non-NULL");
+  layer_row_off[0] = 0;
+  for (int l = 0; l < N; ++l) {
+    int64_t T = 0;
+    for (int h = 0; h < H_kv; ++h) {
+      const int32_t k = K_l[(size_t)l * H_kv + h];
+      if (k < 0) return set_error(KVC_ERR_INVALID_ARG, "K_l[%d][%d] is negative", l, h);
+      T += std::min(k, S);
+    }
+    layer_row_off[l + 1] = layer_row_off[l] + (int64_t)B * T;
+  }
+  return KVC_OK;
+}
+
 int kvc_budget_inverse_stability(int H_kv, const double* s_stable, int64_t total, int lo, int hi, int32_t* K_l_out) {
   if (H_kv < 1 || !s_stable || !K_l_out) return set_error(KVC_ERR_INVALID_ARG, "bad budget arguments");
   if (total < 0 || lo < 0 || hi < lo) return set_error(KVC_ERR_INVALID_ARG, "need total >= 0 and 0 <= lo <= hi");

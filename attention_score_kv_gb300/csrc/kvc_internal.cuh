@@ -116,6 +116,9 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
 // scales of every head into qcode [BH][D] / qscale [BH], then dense scores
 cudaError_t launch_rawdot_int8(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S,
                                int D, int W, int8_t* qcode, float* qscale, float* scores, cudaStream_t st);
+// chunk j of the active layer's keys and values into its full-prompt buffer
+cudaError_t launch_append_chunk(const __nv_bfloat16* k_chunk, const __nv_bfloat16* v_chunk, int B, int H_kv, int S,
+                                int C, int D, int j, __nv_bfloat16* k_act, __nv_bfloat16* v_act, cudaStream_t st);
 // HeteroCache measurement and allocation (overlap coefficient, head
 // similarity, inverse-stability budgets on the device)
 cudaError_t launch_overlap(const int32_t* a, const int64_t* a_off, const int32_t* b, const int64_t* b_off,

@@ -70,6 +70,8 @@ _SIGS = {
     "kvc_overlap_coefficient": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "kvc_head_similarity": (_I, [_P, _P, _I, _I, _P, _P]),
     "kvc_budget_inverse_stability_device": (_I, [_I, _I, _P, _I64, _I, _I, _P, _P]),
+    "kvc_append_chunk": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "kvc_cache_layout": (_I, [_I, _I, _I, _I, _I32P, _I64P]),
     "kvc_retained_layout": (_I, [_I, _I, _I32P, _I64P]),
     "kvc_budget_inverse_stability": (_I, [_I, _F64P, _I64, _I, _I, _I32P]),
     "kvc_check_status": (_I, [_P]),
@@ -150,6 +152,19 @@ def kvc_score_pass2_pool(q_win, k, m, Z, B, H_q, H_kv, S, D, W, b_s, pool_k, sco
 def kvc_score_rawdot_int8(q_win, k, B, H_q, H_kv, S, D, W, scores, ws, ws_bytes=None, stream=None):
     _check(_lib.kvc_score_rawdot_int8(_ptr(q_win), _ptr(k), B, H_q, H_kv, S, D, W, _ptr(scores), _ptr(ws),
                                       ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def kvc_append_chunk(k_chunk, v_chunk, B, H_kv, S, C, D, j, k_act, v_act, stream=None):
+    _check(_lib.kvc_append_chunk(_ptr(k_chunk), _ptr(v_chunk), B, H_kv, S, C, D, j, _ptr(k_act), _ptr(v_act),
+                                 _stream(stream)))
+
+
+def kvc_cache_layout(N, B, H_kv, S, K_l):
+    """Row offsets [N + 1] of each layer in the cross-layer retained cache."""
+    flat = [int(x) for row in K_l for x in row]
+    out = (ctypes.c_int64 * (N + 1))()
+    _check(_lib.kvc_cache_layout(N, B, H_kv, S, _i32(flat), out))
+    return list(out)
 
 
 def kvc_overlap_coefficient(a, a_off, b, b_off, n_pairs, out, stream=None):

@@ -236,6 +236,31 @@ int kvc_budget_inverse_stability_device(int n_layers, int H_kv,
                                         kvc_stream_t stream);
 
 /*
+ * Layer-major chunked prefill (TideKV, Fig. 1(d) and Fig. 2): write the keys
+ * and values of prompt chunk j into the active layer's full-prompt buffer.
+ *   k_chunk, v_chunk  [B, H_kv, c, D] bf16, c = min(C, S - j*C) positions
+ *   k_act, v_act      [B, H_kv, S, D] bf16; positions j*C .. j*C + c - 1 of
+ *                     every (b, head) are overwritten, the rest untouched
+ * 0 <= j*C < S.  After the last chunk, kvc_compress_layer reads k_act/v_act
+ * and may write straight into the cross-layer cache (kvc_cache_layout); the
+ * active buffers are then free for the next layer.
+ */
+int kvc_append_chunk(const kvc_bf16* k_chunk, const kvc_bf16* v_chunk, int B,
+                     int H_kv, int S, int C, int D, int j, kvc_bf16* k_act,
+                     kvc_bf16* v_act, kvc_stream_t stream);
+
+/*
+ * Host helper: rows of the cross-layer retained cache C^[0..N-1] (TideKV,
+ * Fig. 2 and Fig. 4).  Layer l occupies rows layer_row_off[l] ..
+ * layer_row_off[l+1] - 1 of K^ / V^ ([rows, D]) and of the positions, laid out
+ * inside as kvc_retained_layout describes (batch element b at b*T_l).
+ *   K_l            HOST [N][H_kv] budgets (>= 0)
+ *   layer_row_off  HOST [N + 1] out; layer_row_off[N] is the total row count
+ */
+int kvc_cache_layout(int N, int B, int H_kv, int S, const int32_t* K_l,
+                     int64_t* layer_row_off);
+
+/*
  * Host helper: CSR layout of one batch element's retained rows.
  * out_off HOST [H_kv + 1]: head h owns rows out_off[h] .. out_off[h+1]-1,
  * with min(K_l[h], S) rows; out_off[H_kv] is the per-batch-element stride T.

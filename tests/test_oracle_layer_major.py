@@ -1,0 +1,35 @@
+"""Pins of the layer-major prefill oracle (CPU only): chunks reassemble the
+prompt, and the cross-layer cache at TideKV's main setting is the 512 MiB the
+pages report."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import layer_major as LM
+
+
+@pytest.mark.parametrize("S,C", [(700, 128), (512, 128), (5, 8), (1, 1)])
+def test_chunks_reassemble_the_prompt(S, C):
+    rng = np.random.default_rng(S)
+    full = rng.standard_normal((2, 3, S, 4)).astype(np.float32)
+    bounds = LM.chunk_bounds(S, C)
+    assert bounds[0][0] == 0 and bounds[-1][1] == S
+    assert all(b - a == C for a, b in bounds[:-1]) and 0 < bounds[-1][1] - bounds[-1][0] <= C
+    chunks = [full[:, :, a:b] for a, b in bounds]
+    assert np.array_equal(LM.assemble_chunks(chunks, S), full)
+
+
+def test_main_setting_cache_is_512_mib(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "retained_cache_512mib.json")))
+    N, H, K_l, D, B = g["N"], g["H_kv"], g["K_l"], g["D"], g["B"]
+    off = LM.cache_layout(N, B, 65536, [[K_l] * H] * N)
+    assert off[-1] * D * g["elem_bytes"] * 2 == g["bytes"]     # K^ and V^ rows of all layers
+
+
+def test_layout_of_unequal_layers():
+    K_l = [[10, 20, 600], [1, 2, 3]]           # the 600 is clamped to S = 500
+    off = LM.cache_layout(2, 3, 500, K_l)
+    assert off.tolist() == [0, 3 * (10 + 20 + 500), 3 * 530 + 3 * 6]
