@@ -469,6 +469,32 @@ int kvc_cache_layout(int N, int B, int H_kv, int S, const int32_t* K_l, int64_t*
   return KVC_OK;
 }
 
+int kvc_budget_pyramid(int N, int budget, int k_min, int32_t* K_l_out) {
+  if (N < 1 || !K_l_out) return set_error(KVC_ERR_INVALID_ARG, "need N >= 1 and an output array");
+  if (k_min < 0 || k_min > budget) return set_error(KVC_ERR_INVALID_ARG, "need 0 <= k_min <= budget");
+  if (N == 1) {
+    K_l_out[0] = budget;
+    return KVC_OK;
+  }
+  const double k_max = 2.0 * (double)budget - (double)k_min;
+  std::vector<double> rem(N);
+  std::vector<int64_t> base(N);
+  int64_t assigned = 0;
+  for (int l = 0; l < N; ++l) {
+    const double exact = k_max - (k_max - (double)k_min) * (double)l / (double)(N - 1);
+    base[l] = (int64_t)std::floor(exact);
+    rem[l] = exact - (double)base[l];
+    assigned += base[l];
+  }
+  std::vector<int> order(N);
+  for (int l = 0; l < N; ++l) order[l] = l;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return rem[a] > rem[b]; });
+  const int64_t total = (int64_t)N * budget;
+  for (int64_t i = 0; i < total - assigned && i < N; ++i) base[order[i]] += 1;
+  for (int l = 0; l < N; ++l) K_l_out[l] = (int32_t)base[l];
+  return KVC_OK;
+}
+
 int kvc_budget_inverse_stability(int H_kv, const double* s_stable, int64_t total, int lo, int hi, int32_t* K_l_out) {
   if (H_kv < 1 || !s_stable || !K_l_out) return set_error(KVC_ERR_INVALID_ARG, "bad budget arguments");
   if (total < 0 || lo < 0 || hi < lo) return set_error(KVC_ERR_INVALID_ARG, "need total >= 0 and 0 <= lo <= hi");

@@ -72,6 +72,7 @@ _SIGS = {
     "kvc_budget_inverse_stability_device": (_I, [_I, _I, _P, _I64, _I, _I, _P, _P]),
     "kvc_append_chunk": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_cache_layout": (_I, [_I, _I, _I, _I, _I32P, _I64P]),
+    "kvc_budget_pyramid": (_I, [_I, _I, _I, _I32P]),
     "kvc_retained_layout": (_I, [_I, _I, _I32P, _I64P]),
     "kvc_budget_inverse_stability": (_I, [_I, _F64P, _I64, _I, _I, _I32P]),
     "kvc_check_status": (_I, [_P]),
@@ -157,6 +158,12 @@ def kvc_score_rawdot_int8(q_win, k, B, H_q, H_kv, S, D, W, scores, ws, ws_bytes=
 def kvc_append_chunk(k_chunk, v_chunk, B, H_kv, S, C, D, j, k_act, v_act, stream=None):
     _check(_lib.kvc_append_chunk(_ptr(k_chunk), _ptr(v_chunk), B, H_kv, S, C, D, j, _ptr(k_act), _ptr(v_act),
                                  _stream(stream)))
+
+
+def kvc_budget_pyramid(N, budget, k_min):
+    out = (ctypes.c_int32 * N)()
+    _check(_lib.kvc_budget_pyramid(N, budget, k_min, out))
+    return list(out)
 
 
 def kvc_cache_layout(N, B, H_kv, S, K_l):

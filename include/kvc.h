@@ -261,6 +261,17 @@ int kvc_cache_layout(int N, int B, int H_kv, int S, const int32_t* K_l,
                      int64_t* layer_row_off);
 
 /*
+ * Host helper: per-layer budgets that shrink from the first layer to the
+ * last, PyramidKV-style (TideKV's Tables 3-4 run TideKV-PyramidKV at
+ * average budgets 256, 1024 and 4096; the pages give no schedule).  Reading:
+ * a linear ramp from k_max = 2*budget - k_min at layer 0 down to k_min at
+ * layer N-1 (mean = budget), rounded by largest remainder (ties to the
+ * lower layer) so that the layers sum to exactly N * budget.
+ *   K_l_out HOST [N]; 0 <= k_min <= budget.  N = 1 gives budget.
+ */
+int kvc_budget_pyramid(int N, int budget, int k_min, int32_t* K_l_out);
+
+/*
  * Host helper: CSR layout of one batch element's retained rows.
  * out_off HOST [H_kv + 1]: head h owns rows out_off[h] .. out_off[h+1]-1,
  * with min(K_l[h], S) rows; out_off[H_kv] is the per-batch-element stride T.

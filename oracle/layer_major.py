@@ -27,7 +27,7 @@ import numpy as np
 
 from . import kvc_oracle as O
 
-__all__ = ["chunk_bounds", "assemble_chunks", "cache_layout", "compress_prefill"]
+__all__ = ["chunk_bounds", "assemble_chunks", "cache_layout", "compress_prefill", "budgets_pyramid"]
 
 
 def chunk_bounds(S: int, C: int):
@@ -61,3 +61,24 @@ def cache_layout(N: int, B: int, S: int, K_l) -> np.ndarray:
 def compress_prefill(layers, K_l, sink: int, recent: int, pool_k: int):
     """Per layer, kvc_oracle.compress_layer of its full (assembled) KV."""
     return [O.compress_layer(q, k, v, K_l[l], sink, recent, pool_k) for l, (q, k, v) in enumerate(layers)]
+
+
+def budgets_pyramid(N: int, budget: int, k_min: int) -> list:
+    """Per-layer budgets shrinking linearly from 2*budget - k_min to k_min.
+
+    TideKV's Tables 3-4 run a PyramidKV selector at a given average budget;
+    the pages give no schedule.  Reading: a linear ramp with mean = budget,
+    exact shares rounded by largest remainder (ties to the lower layer) so
+    that the layers sum to N * budget.  Parity unpinned beyond that sum, the
+    ramp's ends and its monotonicity.
+    """
+    if N == 1:
+        return [budget]
+    k_max = 2.0 * budget - k_min
+    exact = [k_max - (k_max - k_min) * l / (N - 1) for l in range(N)]
+    base = [int(np.floor(x)) for x in exact]
+    short = N * budget - sum(base)
+    rem = [x - b for x, b in zip(exact, base)]
+    for i in sorted(range(N), key=lambda i: (-rem[i], i))[:short]:
+        base[i] += 1
+    return base

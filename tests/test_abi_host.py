@@ -151,3 +151,18 @@ def test_product_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in re.sub(r"(#|//).*", "", txt), f"{f} mentions the oracle"
+
+
+@pytest.mark.parametrize("N,budget,k_min", [(32, 4096, 1024), (48, 256, 36), (7, 1000, 1000), (1, 512, 100),
+                                            (5, 33, 7)])
+def test_pyramid_budgets_match_oracle(K, N, budget, k_min):
+    from oracle import layer_major as LM
+    assert K.kvc_budget_pyramid(N, budget, k_min) == LM.budgets_pyramid(N, budget, k_min)
+    with pytest.raises(K.KvcError):
+        K.kvc_budget_pyramid(4, 10, 11)
+
+
+def test_cache_layout_matches_oracle(K):
+    from oracle import layer_major as LM
+    K_l = [[100, 300, 9000], [64, 64, 64], [0, 1, 2]]
+    assert K.kvc_cache_layout(3, 2, 3, 8192, K_l) == LM.cache_layout(3, 2, 8192, K_l).tolist()

@@ -33,3 +33,15 @@ def test_layout_of_unequal_layers():
     K_l = [[10, 20, 600], [1, 2, 3]]           # the 600 is clamped to S = 500
     off = LM.cache_layout(2, 3, 500, K_l)
     assert off.tolist() == [0, 3 * (10 + 20 + 500), 3 * 530 + 3 * 6]
+
+
+@pytest.mark.parametrize("N,budget,k_min", [(32, 4096, 1024), (48, 256, 36), (7, 1000, 1000), (1, 512, 100),
+                                            (2, 10, 3), (40, 1024, 0)])
+def test_pyramid_budgets_sum_ends_and_shape(N, budget, k_min):
+    b = LM.budgets_pyramid(N, budget, k_min)
+    assert len(b) == N and sum(b) == N * budget                    # the average budget holds exactly
+    assert all(x >= y for x, y in zip(b, b[1:]))                    # shrinks with depth
+    if N > 1:
+        assert abs(b[0] - (2 * budget - k_min)) <= 1 and abs(b[-1] - k_min) <= 1
+    if k_min == budget:
+        assert b == [budget] * N                                    # no ramp: flat
