@@ -283,7 +283,7 @@ int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, in
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
   auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
-  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, st), "pass 1 launch")))
+  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, true, st), "pass 1 launch")))
     return rc;
   return launch_status(launch_pass1_combine(pm, pz, B, H_q, H_kv, S, W, L.plan, L.gwp, m, Z, st),
                        "pass 1 combine launch");
@@ -399,7 +399,7 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
   auto vv = reinterpret_cast<const __nv_bfloat16*>(v);
   cudaEvent_t* ev = prof_slot();
   if (ev) cudaEventRecord(ev[0], st);
-  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, st), "pass 1 launch")))
+  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, false, st), "pass 1 launch")))
     return rc;
   if (ev) cudaEventRecord(ev[1], st);
   Pass2Out out{nullptr, cand, cnt, L.cap};

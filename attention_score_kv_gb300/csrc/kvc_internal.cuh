@@ -95,9 +95,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // --------------------------------------------------------- kernel launchers
-// pass 1: per-slot partial normalisers (log2-domain max, Z relative to it)
+// pass 1: per-slot partial normalisers (log2-domain reference m, Z relative
+// to it).  exact_max: m is the slot's maximum score (the pass-1 results the
+// API returns); otherwise m is any reference with the same m + log2 Z, which
+// is all the bias of pass 2 needs and skips a max per score.
 cudaError_t launch_pass1(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S, int D,
-                         int W, const ScanPlan& pl, int gwp, float* part_m, float* part_z, cudaStream_t st);
+                         int W, const ScanPlan& pl, int gwp, float* part_m, float* part_z, bool exact_max,
+                         cudaStream_t st);
 cudaError_t launch_pass1_combine(const float* part_m, const float* part_z, int B, int H_q, int H_kv, int S,
                                  int W, const ScanPlan& pl, int gwp, float* m, float* Z, cudaStream_t st);
 // pass 2: lse from (m, Z) (natural units) or from pass-1 partials; output

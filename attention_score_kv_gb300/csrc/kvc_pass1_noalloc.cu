@@ -97,7 +97,7 @@ extern "C" int kvc_score_pass1_noalloc(const kvc_bf16* q_win, const kvc_bf16* k,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
   auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
-  cudaError_t e = launch_pass1(q, kk, B, H_q, H_kv, S, D, W, pl, gwp, pm, pz, st);
+  cudaError_t e = launch_pass1(q, kk, B, H_q, H_kv, S, D, W, pl, gwp, pm, pz, true, st);
   if (e != cudaSuccess) return cuda_error(e, "allocation-free pass 1 launch");
   e = launch_pass1_combine(pm, pz, B, H_q, H_kv, S, W, pl, gwp, m, Z, st);
   if (e != cudaSuccess) return cuda_error(e, "allocation-free pass 1 combine launch");

@@ -7,10 +7,10 @@
 // reads only the key tile from shared memory.  Eight softmax warps read the
 // accumulators from tensor memory: with two blocks each thread owns one
 // query row and all 128 key columns of a tile; with one block the two warps
-// of a lane quarter split the columns.  Each thread keeps a running max (raw
-// dot product units) and the sum of 2^(x - max), x = q.k * log2(e)/sqrt(D),
-// over its segment, then writes the (max * log2(e)/sqrt(D), Z) partial of
-// its row to the segment's slot.
+// of a lane quarter split the columns.  Each thread keeps a reference
+// maximum m (raw dot-product units) and the sum Z of 2^(x - m * c),
+// x = q.k * c, c = log2(e)/sqrt(D), over its segment, then writes the
+// (m * c, Z) partial of its row to the segment's slot.
 #include "kvc_scan_common.cuh"
 
 namespace kvc {
@@ -31,9 +31,39 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;\n" ::
 // waits on parity (u / 3) & 1.
 constexpr uint32_t kP1Bufs = 3;
 constexpr uint32_t kQCol = kP1Bufs * 128;
+constexpr float kBatchSumLimit = 1.152921504606846976e18f;   // 2^60
 
 __device__ __forceinline__ uint32_t p1_buf(uint32_t u) { return u % kP1Bufs; }
 __device__ __forceinline__ uint32_t p1_parity(uint32_t u) { return (u / kP1Bufs) & 1u; }
+
+// Largest of 64 values (a tree, two chains).
+__device__ __forceinline__ float batch_max64(const float* v) {
+  float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+#pragma unroll
+  for (int c = 4; c < 64; c += 4) {
+    mx0 = fmaxf(mx0, fmaxf(v[c], v[c + 1]));
+    mx1 = fmaxf(mx1, fmaxf(v[c + 2], v[c + 3]));
+  }
+  return fmaxf(mx0, mx1);
+}
+
+// Sum of 2^(v * c2 + nm) over 64 values, as two partial sums.
+__device__ __forceinline__ float2 batch_sum64(const float* v, float c2, float nm) {
+  const float2 cc = make_float2(c2, c2), nn = make_float2(nm, nm);
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+  for (int c = 0; c < 64; c += 8) {
+    const float2 x0 = __ffma2_rn(make_float2(v[c], v[c + 1]), cc, nn);
+    const float2 x1 = __ffma2_rn(make_float2(v[c + 2], v[c + 3]), cc, nn);
+    const float2 x2 = __ffma2_rn(make_float2(v[c + 4], v[c + 5]), cc, nn);
+    const float2 x3 = __ffma2_rn(make_float2(v[c + 6], v[c + 7]), cc, nn);
+    a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
+    a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
+    a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
+    a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+  }
+  return __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
+}
 
 template <int D>
 __device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, uint32_t adrain, const Seg* segs, int nseg,
@@ -81,7 +111,7 @@ __device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, uint32_t adrain, co
   }
 }
 
-template <int D, int NMB>
+template <int D, int NMB, bool EXACT_MAX>
 __global__ void __launch_bounds__(kThreads, 1)
 kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap) {
@@ -130,6 +160,9 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       mma_pass1<D>(A, &bars, smem_u32(&adrain), segs, nseg, sQ, sK, tmem, &s_abort);
     }
   } else {
+    // Softmax warps: with two query blocks the four warps of group k read
+    // block k (each thread one query row, all 128 key columns of a tile);
+    // with one block the two warps of a lane quarter split the columns.
     const int e = warp - 2;
     const int quarter = warp & 3;              // TMEM lanes this warp may read
     const int k = e >> 2;                      // 0 or 1
@@ -143,12 +176,14 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
     const int nseg = cta_segments(A, blockIdx.x, segs);
     uint32_t tcount = 0;
     bool ok = true;
-    for (int si = 0; si < nseg && ok; ++si) {
+    // every warp passes the two named barriers of each segment even after a
+    // wait gave up, so none is left waiting there
+    for (int si = 0; si < nseg; ++si) {
       const Seg sg = segs[si];
-      float mrun = -INFINITY;
+      float mref = -INFINITY;
       float2 z2 = make_float2(0.f, 0.f);
       const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
-      for (int ti = 0; ti < ntiles; ++ti, ++tcount) {
+      for (int ti = 0; ti < ntiles && ok; ++ti, ++tcount) {
         const int t = p1_tile_order(ti, ntiles);
         const uint32_t u = NMB == 2 ? 2 * tcount + mb : tcount;   // this warp's sub-tile
         const uint32_t buf = p1_buf(u);
@@ -156,16 +191,16 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         tc::fence_after_sync();
         const uint32_t taddr = tmem + buf * 128 + col0 + ((uint32_t)(quarter * 32) << 16);
         // 64 accumulator columns at a time; the buffer is handed back to the
-        // MMA warp right after the last batch has been read
+        // MMA warp right after the last batch has been read.  Every warp
+        // loads, active or not (a load under a runtime condition costs far
+        // more than the rows an idle warp never uses).
 #pragma unroll 1
         for (int bt = 0; bt < NC / 64; ++bt) {
           float v[64];
-          if (active) {
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) tc::tmem_ld16(taddr + bt * 64 + c, v + c);
-            tc::tmem_wait_ld();
-            tc::reg_fence(v, 64);
-          }
+          for (int c = 0; c < 64; c += 16) tc::tmem_ld16(taddr + bt * 64 + c, v + c);
+          tc::tmem_wait_ld();
+          tc::reg_fence(v, 64);
           if (bt == NC / 64 - 1) {
             tc::fence_before_sync();
             __syncwarp();
@@ -180,51 +215,50 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
               if (j >= sg.b || j > t_row) v[c] = -INFINITY;
             }
           }
-          float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
-#pragma unroll
-          for (int c = 4; c < 64; c += 4) {
-            mx0 = fmaxf(mx0, fmaxf(v[c], v[c + 1]));
-            mx1 = fmaxf(mx1, fmaxf(v[c + 2], v[c + 3]));
-          }
-          const float mx = fmaxf(mx0, mx1);
-          if (mx > mrun) {
-            const float sc = (mrun == -INFINITY) ? 0.f : ex2((mrun - mx) * c2);
-            z2.x *= sc;
-            z2.y *= sc;
-            mrun = mx;
-          }
-          if (mrun > -INFINITY) {
-            const float nm = -mrun * c2;
-            const float2 cc = make_float2(c2, c2), nn = make_float2(nm, nm);
-            float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-#pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-              const float2 x0 = __ffma2_rn(make_float2(v[c], v[c + 1]), cc, nn);
-              const float2 x1 = __ffma2_rn(make_float2(v[c + 2], v[c + 3]), cc, nn);
-              const float2 x2 = __ffma2_rn(make_float2(v[c + 4], v[c + 5]), cc, nn);
-              const float2 x3 = __ffma2_rn(make_float2(v[c + 6], v[c + 7]), cc, nn);
-              a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
-              a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
-              a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
-              a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+          if (EXACT_MAX) {
+            // running maximum: the sum so far is rescaled when it grows
+            const float mx = batch_max64(v);
+            if (mx > mref) {
+              const float sc = (mref == -INFINITY) ? 0.f : ex2((mref - mx) * c2);
+              z2.x *= sc;
+              z2.y *= sc;
+              mref = mx;
             }
-            z2 = __fadd2_rn(z2, __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3)));
+            if (mref > -INFINITY) z2 = __fadd2_rn(z2, batch_sum64(v, c2, -mref * c2));
+            continue;
+          }
+          // The sum is kept relative to a reference mref (raw units): the
+          // first finite batch maximum of the segment.  A batch whose sum
+          // passes 2^60 (a score far above mref) is redone against a raised
+          // reference, so the fp32 state never overflows; any reference gives
+          // the same log-sum-exp.
+          if (mref == -INFINITY) mref = batch_max64(v);
+          if (mref > -INFINITY) {
+            float2 bs = batch_sum64(v, c2, -mref * c2);
+            if (!(bs.x + bs.y <= kBatchSumLimit)) {
+              const float mnew = fmaxf(mref, batch_max64(v));
+              const float sc = ex2((mref - mnew) * c2);
+              z2.x *= sc;
+              z2.y *= sc;
+              mref = mnew;
+              bs = batch_sum64(v, c2, -mref * c2);
+            }
+            z2 = __fadd2_rn(z2, bs);
           }
         }
       }
-      if (!ok) break;
       // segment done: the two column halves of a row (one block) are merged
-      const float2 mine = make_float2(mrun == -INFINITY ? -INFINITY : mrun * c2, z2.x + z2.y);
+      const float2 mine = make_float2(mref == -INFINITY ? -INFINITY : mref * c2, z2.x + z2.y);
       const size_t slot = (size_t)blockIdx.x * A.maxseg + (size_t)(sg.bh - segs[0].bh);
       if (NMB == 2) {
-        if (row < A.gwp16) {
+        if (ok && row < A.gwp16) {
           A.part_m[slot * A.gwp16 + row] = mine.x;
           A.part_z[slot * A.gwp16 + row] = mine.y;
         }
       } else {
         if (k == 1) s_half[quarter * 32 + lane] = mine;
         epi_sync();
-        if (k == 0 && row < A.gwp16) {
+        if (ok && k == 0 && row < A.gwp16) {
           const float2 st = merge_mz(mine, s_half[quarter * 32 + lane]);
           A.part_m[slot * A.gwp16 + row] = st.x;
           A.part_z[slot * A.gwp16 + row] = st.y;
@@ -269,7 +303,8 @@ cudaError_t launch(Kern kernel, int grid, size_t smem, cudaStream_t st, const Sc
 }  // namespace
 
 cudaError_t launch_pass1(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S, int D,
-                         int W, const ScanPlan& pl, int gwp, float* part_m, float* part_z, cudaStream_t st) {
+                         int W, const ScanPlan& pl, int gwp, float* part_m, float* part_z, bool exact_max,
+                         cudaStream_t st) {
   (void)gwp;
   ScanArgs A = base_args(pl, B, H_q, H_kv, S, D, W);
   A.nq = 128 * A.n_mb;
@@ -279,11 +314,19 @@ cudaError_t launch_pass1(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, 
   if (!make_map(&qm, q, D, (uint64_t)B * H_q * W, 1, A.nq) || !make_map(&km, k, D, S, (uint64_t)B * H_kv, kTile))
     return cudaErrorInvalidValue;
   const size_t smem = pipe_smem(D, A.nq);
-  if (D == 64)
-    return A.n_mb == 2 ? launch(kvc_tc_pass1_kernel<64, 2>, pl.P, smem, st, A, qm, km)
-                       : launch(kvc_tc_pass1_kernel<64, 1>, pl.P, smem, st, A, qm, km);
-  return A.n_mb == 2 ? launch(kvc_tc_pass1_kernel<128, 2>, pl.P, smem, st, A, qm, km)
-                     : launch(kvc_tc_pass1_kernel<128, 1>, pl.P, smem, st, A, qm, km);
+  const bool two = A.n_mb == 2;
+  if (D == 64) {
+    if (exact_max)
+      return two ? launch(kvc_tc_pass1_kernel<64, 2, true>, pl.P, smem, st, A, qm, km)
+                 : launch(kvc_tc_pass1_kernel<64, 1, true>, pl.P, smem, st, A, qm, km);
+    return two ? launch(kvc_tc_pass1_kernel<64, 2, false>, pl.P, smem, st, A, qm, km)
+               : launch(kvc_tc_pass1_kernel<64, 1, false>, pl.P, smem, st, A, qm, km);
+  }
+  if (exact_max)
+    return two ? launch(kvc_tc_pass1_kernel<128, 2, true>, pl.P, smem, st, A, qm, km)
+               : launch(kvc_tc_pass1_kernel<128, 1, true>, pl.P, smem, st, A, qm, km);
+  return two ? launch(kvc_tc_pass1_kernel<128, 2, false>, pl.P, smem, st, A, qm, km)
+             : launch(kvc_tc_pass1_kernel<128, 1, false>, pl.P, smem, st, A, qm, km);
 }
 
 cudaError_t launch_pass1_combine(const float* part_m, const float* part_z, int B, int H_q, int H_kv, int S, int W,

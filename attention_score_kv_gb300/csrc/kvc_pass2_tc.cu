@@ -31,6 +31,7 @@ constexpr int kPoolWarp = 2 + 2 * kGroupWarps;   // warp 10
 constexpr int kThreads = 32 * (kPoolWarp + 1);
 constexpr int kRing = 4;
 constexpr int kRingPad = 16;                     // room for the previous tile's last 2h masses
+static_assert(kMaxPool - 1 <= kRingPad, "the pooling halo must fit the ring pad");
 constexpr float kNoWeight = -1.0e30f;            // bias of padding rows: weight 0
 
 struct RingBars {
@@ -303,10 +304,12 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll 1
         for (int bt = 0; bt < nbt; ++bt) {
+          // all four column chunks are loaded even past the last one in use
+          // (they stay inside this group's 256-column buffer): a load under a
+          // runtime condition costs far more than the unused columns
           float v[64];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (4 * bt + i < nch) tc::tmem_ld16(taddr + (4 * bt + i) * 16, v + 16 * i);
+          for (int i = 0; i < 4; ++i) tc::tmem_ld16(taddr + (4 * bt + i) * 16, v + 16 * i);
           tc::tmem_wait_ld();
           tc::reg_fence(v, 64);
           if (bt == nbt - 1) {
@@ -315,22 +318,26 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
             if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[g]));
           }
           if (!need_mask) {
+            // a ragged last batch: its unused columns weigh 2^-inf = 0, so
+            // the 64 columns below run as one unguarded block
+            if (4 * bt + 4 > nch) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (4 * bt + i < nch) {
+              for (int i = 0; i < 4; ++i)
+                if (4 * bt + i >= nch) {
 #pragma unroll
-                for (int q = 0; q < 16; q += 8) {
-                  const float* w = v + 16 * i + q;
-                  const float2 x0 = __fmul2_rn(make_float2(w[0], w[1]), cc);
-                  const float2 x1 = __fmul2_rn(make_float2(w[2], w[3]), cc);
-                  const float2 x2 = __fmul2_rn(make_float2(w[4], w[5]), cc);
-                  const float2 x3 = __fmul2_rn(make_float2(w[6], w[7]), cc);
-                  a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
-                  a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
-                  a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
-                  a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+                  for (int q = 0; q < 16; ++q) v[16 * i + q] = -INFINITY;
                 }
-              }
+            }
+#pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+              const float2 x0 = __fmul2_rn(make_float2(v[c], v[c + 1]), cc);
+              const float2 x1 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), cc);
+              const float2 x2 = __fmul2_rn(make_float2(v[c + 4], v[c + 5]), cc);
+              const float2 x3 = __fmul2_rn(make_float2(v[c + 6], v[c + 7]), cc);
+              a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
+              a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
+              a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
+              a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
             }
           } else {
             // tiles near the window: window query i (column g*W + i) sees key
@@ -384,13 +391,20 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
           __syncwarp();
         }
         if (!wait_bar_warp(smem_u32(&rbars.rfull[slot]), (tcount / kRing) & 1, &s_abort, A.status)) { ok = false; break; }
-        // lane l pools keys t0 - h + 4l + k, k = 0..3, over masses win[k .. k + 2h]
+        // lane l pools keys t0 - h + 4l + k, k = 0..3, over masses win[k .. k + 2h]:
+        // the 4 + 2h masses are loaded into registers first, then summed in
+        // ascending order, so no add waits on a shared-memory load
         const float* win = rr + kRingPad - 2 * hw + 4 * lane;
+        float wv[4 + kRingPad];
+#pragma unroll
+        for (int i = 0; i < 4 + kRingPad; ++i) wv[i] = (i < 4 + 2 * hw) ? win[i] : 0.f;
         float sc[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           float acc = 0.f;
-          for (int d = 0; d <= 2 * hw; ++d) acc += win[k + d];
+#pragma unroll
+          for (int d = 0; d <= kRingPad; ++d)
+            if (d <= 2 * hw) acc += wv[k + d];
           sc[k] = A.pool_k == 1 ? acc : acc * inv_pool;
         }
         const int j0 = t0 - hw + 4 * lane;
