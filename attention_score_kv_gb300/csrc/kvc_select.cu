@@ -347,20 +347,35 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
   cluster_sync_all();
 
   // keys taken by the lower-ranked CTAs of the head: all above T and, of
-  // the ties, as many as were still needed in key order
-  if (threadIdx.x == 0) {
-    int ob = 0, eb = 0;
-    for (int r = 0; r < rank; ++r) {
-      const int g = (int)ld_dsmem_u32(dsmem_addr(&cs.cta_gt, (uint32_t)r));
-      const int e = (int)ld_dsmem_u32(dsmem_addr(&cs.cta_eq, (uint32_t)r));
-      ob += g + (mode == 2 ? 0 : max(0, min(e, need_eq - eb)));
-      eb += e;
+  // the ties, as many as were still needed in key order.  Lane r of warp 0
+  // reads CTA r's counts (all remote loads in flight together); the ties
+  // seen before r come from a prefix sum.
+  if (threadIdx.x < 32) {
+    const int r = (int)threadIdx.x;
+    int g = 0, e = 0;
+    if (r < rank) {
+      g = (int)ld_dsmem_u32(dsmem_addr(&cs.cta_gt, (uint32_t)r));
+      e = (int)ld_dsmem_u32(dsmem_addr(&cs.cta_eq, (uint32_t)r));
     }
-    for (int q = 0; q < kClWarps; ++q) {
-      cs.wout[q] = ob;
-      cs.weqb[q] = eb;
-      ob += cs.wgt[q] + (mode == 2 ? 0 : max(0, min(cs.weq[q], need_eq - eb)));
-      eb += cs.weq[q];
+    int e_incl = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, e_incl, o);
+      if (r >= o) e_incl += t;
+    }
+    const int e_before = e_incl - e;
+    int took = r < rank ? g + (mode == 2 ? 0 : max(0, min(e, need_eq - e_before))) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) took += __shfl_xor_sync(0xffffffffu, took, o);
+    const int eb_all = __shfl_sync(0xffffffffu, e_incl, 31);
+    if (threadIdx.x == 0) {
+      int ob = took, eb = eb_all;
+      for (int q = 0; q < kClWarps; ++q) {
+        cs.wout[q] = ob;
+        cs.weqb[q] = eb;
+        ob += cs.wgt[q] + (mode == 2 ? 0 : max(0, min(cs.weq[q], need_eq - eb)));
+        eb += cs.weq[q];
+      }
     }
   }
   __syncthreads();
