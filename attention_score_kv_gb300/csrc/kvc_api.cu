@@ -236,6 +236,71 @@ int launch_status(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace {
+
+// kvc_compress_layer with an optional event the gather waits on (the values
+// are read by the gather only).
+int compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int D, int W, const int32_t* K_l,
+                   int sink, int recent, int pool_k, int b_s, const kvc_bf16* q_win, const kvc_bf16* k,
+                   const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, void* ws,
+                   size_t ws_bytes, cudaEvent_t v_ready, kvc_stream_t stream) {
+  int rc;
+  if (N < 1 || layer < 0 || layer >= N) return set_error(KVC_ERR_INVALID_ARG, "layer %d outside [0, N=%d)", layer, N);
+  if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s)) || (rc = check_pool(pool_k))) return rc;
+  if (C < W || C > S) return set_error(KVC_ERR_INVALID_ARG, "chunk C=%d must satisfy W=%d <= C <= S=%d", C, W, S);
+  if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(v, 16, "v")) ||
+      (rc = check_ptr(k_out, 16, "k_out")) || (rc = check_ptr(v_out, 16, "v_out")) ||
+      (rc = check_ptr(pos_out, 4, "pos_out")))
+    return rc;
+  SelParams sp;
+  int kmax = 0;
+  if ((rc = make_sel(S, H_kv, K_l, sink, recent, &sp, &kmax))) return rc;
+  WsLayout L;
+  if (!layout_ws(B, H_q, H_kv, D, W, b_s, kmax, pool_k, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
+  if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
+  sp.nparts = L.plan.nparts;
+  sp.L = L.plan.L;
+  sp.maxseg = L.plan.maxseg;
+  char* w = static_cast<char*>(ws);
+  float* pm = reinterpret_cast<float*>(w + L.off_part_m);
+  float* pz = reinterpret_cast<float*>(w + L.off_part_z);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(w + L.off_cand);
+  int* cnt = reinterpret_cast<int*>(w + L.off_cand_cnt);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
+  auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
+  auto vv = reinterpret_cast<const __nv_bfloat16*>(v);
+  cudaEvent_t* ev = prof_slot();
+  if (ev) cudaEventRecord(ev[0], st);
+  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, false, st), "pass 1 launch")))
+    return rc;
+  if (ev) cudaEventRecord(ev[1], st);
+  Pass2Out out{nullptr, cand, cnt, L.cap};
+  float* bias = reinterpret_cast<float*>(w + L.off_bias);
+  if ((rc = launch_status(launch_pass2(q, kk, nullptr, nullptr, pm, pz, bias, B, H_q, H_kv, S, D, W, pool_k, L.plan,
+                                       L.gwp, &sp, out, true, st),
+                          "pass 2 launch")))
+    return rc;
+  if (ev) cudaEventRecord(ev[2], st);
+  if ((rc = launch_status(launch_select(1, nullptr, cand, cnt, L.cap, B, sp, pos_out, st),
+                          "selection launch")))
+    return rc;
+  if (ev) cudaEventRecord(ev[3], st);
+  std::vector<int64_t> off(H_kv + 1);
+  for (int h = 0; h < H_kv; ++h) off[h] = sp.off[h];
+  off[H_kv] = sp.T;
+  if (v_ready && (rc = launch_status(cudaStreamWaitEvent(st, v_ready, 0), "wait for v_ready")))
+    return rc;
+  rc = launch_status(launch_gather(kk, vv, pos_out, B, H_kv, S, D, sp.T, off.data(),
+                                   reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out),
+                                   pos_out, st),
+                     "gather launch");
+  if (ev) cudaEventRecord(ev[4], st);
+  return rc;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* kvc_last_error(void) { return t_err; }
@@ -371,57 +436,17 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv,
                        int sink, int recent, int pool_k, int b_s, const kvc_bf16* q_win, const kvc_bf16* k,
                        const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, void* ws,
                        size_t ws_bytes, kvc_stream_t stream) {
-  int rc;
-  if (N < 1 || layer < 0 || layer >= N) return set_error(KVC_ERR_INVALID_ARG, "layer %d outside [0, N=%d)", layer, N);
-  if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s)) || (rc = check_pool(pool_k))) return rc;
-  if (C < W || C > S) return set_error(KVC_ERR_INVALID_ARG, "chunk C=%d must satisfy W=%d <= C <= S=%d", C, W, S);
-  if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(v, 16, "v")) ||
-      (rc = check_ptr(k_out, 16, "k_out")) || (rc = check_ptr(v_out, 16, "v_out")) ||
-      (rc = check_ptr(pos_out, 4, "pos_out")))
-    return rc;
-  SelParams sp;
-  int kmax = 0;
-  if ((rc = make_sel(S, H_kv, K_l, sink, recent, &sp, &kmax))) return rc;
-  WsLayout L;
-  if (!layout_ws(B, H_q, H_kv, D, W, b_s, kmax, pool_k, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
-  if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
-  sp.nparts = L.plan.nparts;
-  sp.L = L.plan.L;
-  sp.maxseg = L.plan.maxseg;
-  char* w = static_cast<char*>(ws);
-  float* pm = reinterpret_cast<float*>(w + L.off_part_m);
-  float* pz = reinterpret_cast<float*>(w + L.off_part_z);
-  uint64_t* cand = reinterpret_cast<uint64_t*>(w + L.off_cand);
-  int* cnt = reinterpret_cast<int*>(w + L.off_cand_cnt);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  auto q = reinterpret_cast<const __nv_bfloat16*>(q_win);
-  auto kk = reinterpret_cast<const __nv_bfloat16*>(k);
-  auto vv = reinterpret_cast<const __nv_bfloat16*>(v);
-  cudaEvent_t* ev = prof_slot();
-  if (ev) cudaEventRecord(ev[0], st);
-  if ((rc = launch_status(launch_pass1(q, kk, B, H_q, H_kv, S, D, W, L.plan, L.gwp, pm, pz, false, st), "pass 1 launch")))
-    return rc;
-  if (ev) cudaEventRecord(ev[1], st);
-  Pass2Out out{nullptr, cand, cnt, L.cap};
-  float* bias = reinterpret_cast<float*>(w + L.off_bias);
-  if ((rc = launch_status(launch_pass2(q, kk, nullptr, nullptr, pm, pz, bias, B, H_q, H_kv, S, D, W, pool_k, L.plan,
-                                       L.gwp, &sp, out, true, st),
-                          "pass 2 launch")))
-    return rc;
-  if (ev) cudaEventRecord(ev[2], st);
-  if ((rc = launch_status(launch_select(1, nullptr, cand, cnt, L.cap, B, sp, pos_out, st),
-                          "selection launch")))
-    return rc;
-  if (ev) cudaEventRecord(ev[3], st);
-  std::vector<int64_t> off(H_kv + 1);
-  for (int h = 0; h < H_kv; ++h) off[h] = sp.off[h];
-  off[H_kv] = sp.T;
-  rc = launch_status(launch_gather(kk, vv, pos_out, B, H_kv, S, D, sp.T, off.data(),
-                                   reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out),
-                                   pos_out, st),
-                     "gather launch");
-  if (ev) cudaEventRecord(ev[4], st);
-  return rc;
+  return compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, pool_k, b_s, q_win, k, v, k_out,
+                        v_out, pos_out, ws, ws_bytes, nullptr, stream);
+}
+
+int kvc_compress_layer_deferred_v(int N, int layer, int B, int S, int C, int H_q, int H_kv, int D, int W,
+                                  const int32_t* K_l, int sink, int recent, int pool_k, int b_s,
+                                  const kvc_bf16* q_win, const kvc_bf16* k, const kvc_bf16* v, kvc_bf16* k_out,
+                                  kvc_bf16* v_out, int32_t* pos_out, void* ws, size_t ws_bytes,
+                                  kvc_event_t v_ready, kvc_stream_t stream) {
+  return compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, pool_k, b_s, q_win, k, v, k_out,
+                        v_out, pos_out, ws, ws_bytes, reinterpret_cast<cudaEvent_t>(v_ready), stream);
 }
 
 int kvc_retained_layout(int H_kv, int S, const int32_t* K_l, int64_t* out_off) {

@@ -67,6 +67,8 @@ _SIGS = {
     "kvc_gather": (_I, [_P, _P, _P, _I, _I, _I, _I, _I32P, _P, _P, _P, _P]),
     "kvc_compress_layer": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I32P, _I, _I, _I, _I,
                                 _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "kvc_compress_layer_deferred_v": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I32P, _I, _I, _I, _I,
+                                           _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "kvc_overlap_coefficient": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "kvc_head_similarity": (_I, [_P, _P, _I, _I, _P, _P]),
     "kvc_budget_inverse_stability_device": (_I, [_I, _I, _P, _I64, _I, _I, _P, _P]),
@@ -203,6 +205,22 @@ def kvc_compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, po
     _check(_lib.kvc_compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, _i32(K_l), sink, recent, pool_k, b_s,
                                    _ptr(q_win), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out), _ptr(pos_out),
                                    _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def _event(ev) -> int | None:
+    if ev is None or isinstance(ev, int):
+        return ev
+    return ev.cuda_event   # torch.cuda.Event: its cudaEvent_t (0 until first recorded)
+
+
+def kvc_compress_layer_deferred_v(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, pool_k, b_s, q_win, k, v,
+                                  k_out, v_out, pos_out, ws, v_ready, ws_bytes=None, stream=None):
+    """kvc_compress_layer whose gather first waits on the event v_ready
+    (e.g. recorded after v's host-to-device copy on another stream)."""
+    _check(_lib.kvc_compress_layer_deferred_v(N, layer, B, S, C, H_q, H_kv, D, W, _i32(K_l), sink, recent, pool_k,
+                                              b_s, _ptr(q_win), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out),
+                                              _ptr(pos_out), _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
+                                              _event(v_ready), _stream(stream)))
 
 
 def kvc_retained_layout(H_kv, S, K_l) -> list:

@@ -456,22 +456,45 @@ def main():
                              ko=torch.empty(L["k_out"].shape, dtype=torch.bfloat16).pin_memory(),
                              vo=torch.empty(L["v_out"].shape, dtype=torch.bfloat16).pin_memory(),
                              po=torch.empty(L["pos"].shape, dtype=torch.int32).pin_memory()))
-        dq = torch.empty_like(layers[0]["q"])
-        dk = torch.empty_like(layers[0]["k"])
-        dv = torch.empty_like(layers[0]["v"])
+        # Two slots of device buffers (steps alternate), so a step never
+        # overwrites what the previous one still reads.  Per step: Q and K go
+        # up on the main stream, then V on a side stream (after K, so the
+        # host link carries one copy at a time) while the scans run; only
+        # the gather waits for V (kvc_compress_layer_deferred_v).  The
+        # outputs come down on a third stream, overlapping the next step's
+        # uploads.
+        dev_in = [dict(q=torch.empty_like(layers[0]["q"]), k=torch.empty_like(layers[0]["k"]),
+                       v=torch.empty_like(layers[0]["v"])) for _ in range(nl_e)]
+        s_v = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        ev_k = [torch.cuda.Event() for _ in range(nl_e)]
+        ev_v = [torch.cuda.Event() for _ in range(nl_e)]
+        ev_done = [torch.cuda.Event() for _ in range(nl_e)]
+        ev_out = [torch.cuda.Event() for _ in range(nl_e)]
+        for e in ev_out:
+            e.record(s_out)
 
         def e2e_step(i):
-            H = host[i % nl_e]
-            L = layers[i % nl_e]
-            dq.copy_(H["q"], non_blocking=True)
-            dk.copy_(H["k"], non_blocking=True)
-            dv.copy_(H["v"], non_blocking=True)
-            K.kvc_compress_layer(cfg.N, L["id"], cfg.B, cfg.S, cfg.C, cfg.H_q, cfg.H_kv, cfg.D, cfg.W, L["K_l"],
-                                 cfg.sink, cfg.recent, cfg.pool_k, cfg.b_s, dq, dk, dv, L["k_out"], L["v_out"],
-                                 L["pos"], ws, stream=stream)
-            H["ko"].copy_(L["k_out"], non_blocking=True)
-            H["vo"].copy_(L["v_out"], non_blocking=True)
-            H["po"].copy_(L["pos"], non_blocking=True)
+            p = i % nl_e
+            H, L, Dv = host[p], layers[p], dev_in[p]
+            stream.wait_event(ev_out[p])                 # slot p's outputs have been copied out
+            Dv["q"].copy_(H["q"], non_blocking=True)
+            Dv["k"].copy_(H["k"], non_blocking=True)
+            ev_k[p].record(stream)
+            s_v.wait_event(ev_k[p])                      # after K (and after the gather that last read slot p)
+            with torch.cuda.stream(s_v):
+                Dv["v"].copy_(H["v"], non_blocking=True)
+            ev_v[p].record(s_v)
+            K.kvc_compress_layer_deferred_v(cfg.N, L["id"], cfg.B, cfg.S, cfg.C, cfg.H_q, cfg.H_kv, cfg.D, cfg.W,
+                                            L["K_l"], cfg.sink, cfg.recent, cfg.pool_k, cfg.b_s, Dv["q"], Dv["k"],
+                                            Dv["v"], L["k_out"], L["v_out"], L["pos"], ws, ev_v[p], stream=stream)
+            ev_done[p].record(stream)
+            s_out.wait_event(ev_done[p])
+            with torch.cuda.stream(s_out):
+                H["ko"].copy_(L["k_out"], non_blocking=True)
+                H["vo"].copy_(L["v_out"], non_blocking=True)
+                H["po"].copy_(L["pos"], non_blocking=True)
+            ev_out[p].record(s_out)
 
         for i in range(2):
             e2e_step(i)
@@ -483,6 +506,8 @@ def main():
         a0.record(stream)
         for i in range(args.e2e_steps):
             e2e_step(i)
+        stream.wait_stream(s_out)                        # the last outputs are on the host
+        stream.wait_stream(s_v)
         a1.record(stream)
         torch.cuda.synchronize(dev)
         ems = a0.elapsed_time(a1)

@@ -46,6 +46,7 @@ extern "C" {
 
 typedef uint16_t kvc_bf16;                 /* raw bfloat16 bits */
 typedef struct CUstream_st* kvc_stream_t;  /* the same type as cudaStream_t */
+typedef struct CUevent_st* kvc_event_t;    /* the same type as cudaEvent_t */
 
 enum kvc_status_code {
   KVC_OK = 0,
@@ -191,6 +192,27 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q,
                        const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out,
                        int32_t* pos_out, void* ws, size_t ws_bytes,
                        kvc_stream_t stream);
+
+/*
+ * kvc_compress_layer for callers that upload the values while the scans
+ * run.  In the compress only the final gather reads v (pass 1, pass 2 and
+ * the selection read q_win and k).  Here the gather first waits on v_ready:
+ * an event the caller records after v is complete, typically on the stream
+ * that copies v from the host, so that the copy overlaps the scans.
+ *   v_ready  caller-owned CUDA event, or NULL for no wait (then this call
+ *            is kvc_compress_layer itself).  The library only waits on it
+ *            (cudaStreamWaitEvent on `stream`) and does not keep it.
+ * Arguments, results and errors otherwise as kvc_compress_layer; q_win and
+ * k must be complete in stream order, as there.
+ */
+int kvc_compress_layer_deferred_v(int N, int layer, int B, int S, int C,
+                                  int H_q, int H_kv, int D, int W,
+                                  const int32_t* K_l, int sink, int recent,
+                                  int pool_k, int b_s, const kvc_bf16* q_win,
+                                  const kvc_bf16* k, const kvc_bf16* v,
+                                  kvc_bf16* k_out, kvc_bf16* v_out,
+                                  int32_t* pos_out, void* ws, size_t ws_bytes,
+                                  kvc_event_t v_ready, kvc_stream_t stream);
 
 /*
  * Overlap coefficient of index sets (HeteroCache, "Key Contributions" 1 and
