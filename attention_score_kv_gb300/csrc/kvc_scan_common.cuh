@@ -157,6 +157,7 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
   Seg segs[kMaxSegs];
   const int nseg = cta_segments(A, blockIdx.x, segs);
   const int G = A.H_q / A.H_kv;
+  const uint64_t k_policy = PASS == 2 ? tc::l2_evict_first_policy() : 0ull;
   uint32_t stage = 0, phase = 0, qphase = 0;
   for (int si = 0; si < nseg; ++si) {
     const Seg sg = segs[si];
@@ -176,9 +177,14 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
       if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, A.status)) return;
       const uint32_t dst = sK + stage * kTileBytes;
       tc::mbar_arrive_expect_tx(smem_u32(&bars->full[stage]), kTileBytes);
-      for (int kh = 0; kh < NKH; ++kh)
-        tc::tma_load_3d(dst + kh * (kTile * 128), kmap, smem_u32(&bars->full[stage]), kh * 64, start + t * kTile,
-                        sg.bh);
+      for (int kh = 0; kh < NKH; ++kh) {
+        if (PASS == 2)   // the last full read of the keys: evict them first, keep the candidate lists in L2
+          tc::tma_load_3d_hint(dst + kh * (kTile * 128), kmap, smem_u32(&bars->full[stage]), kh * 64,
+                               start + t * kTile, sg.bh, k_policy);
+        else
+          tc::tma_load_3d(dst + kh * (kTile * 128), kmap, smem_u32(&bars->full[stage]), kh * 64, start + t * kTile,
+                          sg.bh);
+      }
       if (++stage == NST) { stage = 0; phase ^= 1; }
     }
   }
