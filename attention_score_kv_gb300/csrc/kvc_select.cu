@@ -95,6 +95,7 @@ struct __align__(16) ClSmem {
   int scan[32];
   int digit, need;
   int wgt[kClWarps], weq[kClWarps], wout[kClWarps], weqb[kClWarps];
+  int wsurv[kClWarps], nsurv;                // keys that share the round-0 digit: per warp, in total
   int cta_gt, cta_eq;                        // this CTA's keys above / at the threshold
 };
 
@@ -150,6 +151,60 @@ __device__ void cl_hist(const HeadView& hv, const uint64_t* stage, int f0, int n
     const unsigned peers = __match_any_sync(0xffffffffu, bin);
     if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
   }
+}
+
+// This CTA's histogram of round `round` over the survivors of round 0 (their
+// score bits, in any order).
+__device__ void cl_hist_surv(const uint32_t* surv, int ns, int round, uint32_t prefix, uint32_t* h) {
+  for (int i0 = 0; i0 < ns; i0 += kClThreads) {
+    const int i = i0 + threadIdx.x;
+    const int bin = i < ns ? radix_bin(surv[i], round, prefix) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  }
+}
+
+// After round 0: the score bits of this CTA's keys whose top 11 bits equal
+// d0 are copied, in key order, into surv (the round-0 histogram, which no
+// CTA reads any more), when they fit; returns their number, or -1 when they
+// do not fit and the later rounds scan the whole share.
+__device__ int cl_survivors(const HeadView& hv, const uint64_t* stage, int f0, int n, uint32_t d0, ClSmem* cs,
+                            uint32_t* surv, int cap) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int chunk = (n + kClWarps - 1) / kClWarps;
+  const int lo = min(n, w * chunk), hi = min(n, lo + chunk);
+  int cnt = 0;
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const bool keep = i < hi && (uint32_t)(share_entry(hv, stage, f0, n, i) >> 53) == d0;
+    cnt += __popc(__ballot_sync(0xffffffffu, keep));
+  }
+  if (lane == 0) cs->wsurv[w] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int q = 0; q < kClWarps; ++q) {
+      const int c = cs->wsurv[q];
+      cs->wsurv[q] = t;
+      t += c;
+    }
+    cs->nsurv = t;
+  }
+  __syncthreads();
+  const int total = cs->nsurv;
+  if (total > cap) return -1;
+  int pos = cs->wsurv[w];
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i0 = lo; i0 < hi; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t u = i < hi ? (uint32_t)(share_entry(hv, stage, f0, n, i) >> 32) : 0u;
+    const bool keep = i < hi && (u >> 21) == d0;
+    const unsigned b = __ballot_sync(0xffffffffu, keep);
+    if (keep) surv[pos + __popc(b & lt)] = u;
+    pos += __popc(b);
+  }
+  __syncthreads();
+  return total;
 }
 
 // Sum round `round`'s histograms over the cluster and find the digit that
@@ -304,9 +359,14 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
   if (mode == 1) {
     uint32_t prefix = 0u;
     int need = n_sel;
+    int ns = -1;   // survivors of round 0 held in cs.hist[0 .. kHist1), or -1: scan the share
     for (int round = 0; round < 3; ++round) {
       uint32_t* hr = cs.hist + (round == 0 ? 0 : round == 1 ? kHist1 : kHist1 + kHist2);
-      cl_hist(hv, stage, f0, n, round, prefix, hr);
+      if (round == 1) ns = cl_survivors(hv, stage, f0, n, prefix, &cs, cs.hist, kHist1);
+      if (round > 0 && ns >= 0)
+        cl_hist_surv(cs.hist, ns, round, prefix, hr);
+      else
+        cl_hist(hv, stage, f0, n, round, prefix, hr);
       cluster_sync_all();
       int d, nd;
       cl_resolve<kCl>(&cs, round, need, &d, &nd);
