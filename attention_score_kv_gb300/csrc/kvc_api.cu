@@ -101,12 +101,12 @@ ScanPlan plan_for(int BH, int S, int P) {
   pl.L = L;
   int maxseg = 1;
   for (int64_t c = 0; c < p; ++c) {
-    const int64_t f0 = c * L, f1 = std::min(f0 + L, total);
-    maxseg = std::max<int>(maxseg, (int)((f1 - 1) / S - f0 / S + 1));
+    const int64_t f0 = range_begin(c, L, S, total), f1 = range_begin(c + 1, L, S, total);
+    if (f1 > f0) maxseg = std::max<int>(maxseg, (int)((f1 - 1) / S - f0 / S + 1));
   }
   int nparts = 1;
   for (int64_t h = 0; h < BH; ++h)
-    nparts = std::max<int>(nparts, (int)(((h + 1) * S - 1) / L - (h * S) / L + 1));
+    nparts = std::max<int>(nparts, (int)(range_of((h + 1) * S - 1, L, S, total) - range_of(h * S, L, S, total) + 1));
   pl.maxseg = maxseg;
   pl.nparts = nparts;
   return pl;
@@ -261,6 +261,7 @@ int compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int
   sp.nparts = L.plan.nparts;
   sp.L = L.plan.L;
   sp.maxseg = L.plan.maxseg;
+  sp.total = (int64_t)B * H_kv * S;
   char* w = static_cast<char*>(ws);
   float* pm = reinterpret_cast<float*>(w + L.off_part_m);
   float* pz = reinterpret_cast<float*>(w + L.off_part_z);

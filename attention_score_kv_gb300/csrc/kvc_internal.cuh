@@ -28,9 +28,10 @@ constexpr int kStatusTimeout = 3;
 constexpr int kStatusBadInput = 4;      // a device-resident input broke the contract
 
 // How the flattened key space [B*H_kv][S] is cut into scan CTAs: CTA c owns
-// keys [c*L, (c+1)*L) and touches at most `maxseg` KV heads; one head is
-// touched by at most `nparts` CTAs.  Per-(CTA, head) "slots" hold pass-1
-// partials and pass-2 candidate lists: slot = c * maxseg + (head - first head of c).
+// keys [range_begin(c), range_begin(c + 1)) and touches at most `maxseg` KV
+// heads; one head is touched by at most `nparts` CTAs.  Per-(CTA, head)
+// "slots" hold pass-1 partials and pass-2 candidate lists:
+// slot = c * maxseg + (head - first head of c).
 struct ScanPlan {
   int P;
   int64_t L;
@@ -52,8 +53,34 @@ struct WsLayout {
 };
 
 // Per-head selection parameters, passed by value in the kernel argument block.
+// Start of scan CTA c's key range: c*L, moved onto the nearest head
+// boundary when it lies within min(L/4, kSnapKeys) keys of one.  A CTA that
+// would end with a sliver of the next head (or start with the tail of the
+// previous one) pays a whole segment switch for it (the queries reloaded,
+// the pipeline drained and refilled), several times the cost of a few more
+// tiles.  The ranges stay ordered and at least L/2 long.
+constexpr int64_t kSnapKeys = 4 * kTile;
+__host__ __device__ inline int64_t range_begin(int64_t c, int64_t L, int64_t S, int64_t total) {
+  const int64_t f = c * L;
+  if (f <= 0) return 0;
+  if (f >= total) return total;
+  const int64_t snap = L / 4 < kSnapKeys ? L / 4 : kSnapKeys;
+  const int64_t r = f % S;
+  if (r != 0 && r <= snap) return f - r;
+  if (r != 0 && S - r <= snap) return f + (S - r) < total ? f + (S - r) : total;
+  return f;
+}
+// The scan CTA whose range holds key f, 0 <= f < total.
+__host__ __device__ inline int64_t range_of(int64_t f, int64_t L, int64_t S, int64_t total) {
+  int64_t c = f / L;
+  if (f < range_begin(c, L, S, total)) --c;
+  else if (f >= range_begin(c + 1, L, S, total)) ++c;
+  return c;
+}
+
 struct SelParams {
   int S, sink, recent, H_kv, nparts;
+  int64_t total;        // B * H_kv * S: the flattened key space of the scan plan
   int r_lo;             // min(sink, S): mandatory keys at the front
   int r_hi;             // max(S - recent, r_lo): first mandatory key at the back
   int64_t T;            // retained rows per batch element

@@ -488,12 +488,12 @@ __global__ void kvc_lse_bias_kernel(const __grid_constant__ ScanArgs A, float* _
       const size_t src = (size_t)(b * A.H_q + h * G) * A.W + r;
       lse2 = A.m_in[src] * kLog2e + log2f(A.z_in[src]);
     } else {
-      const int64_t S = A.S;
-      const int c_first = (int)(((int64_t)bh * S) / A.L);
-      const int c_last = (int)((((int64_t)bh + 1) * S - 1) / A.L);
+      const int64_t S = A.S, total = (int64_t)A.B * A.H_kv * A.S;
+      const int c_first = (int)range_of((int64_t)bh * S, A.L, S, total);
+      const int c_last = (int)range_of(((int64_t)bh + 1) * S - 1, A.L, S, total);
       float2 st = make_float2(-INFINITY, 0.f);
       for (int c = c_first + lane; c <= c_last; c += 32) {
-        const int seg = bh - (int)(((int64_t)c * A.L) / S);
+        const int seg = bh - (int)(range_begin(c, A.L, S, total) / S);
         const size_t o = ((size_t)c * A.maxseg + seg) * A.gwp16 + r;
         st = merge_mz(st, make_float2(A.pm_in[o], A.pz_in[o]));
       }

@@ -3,9 +3,11 @@
 // tensor-map set-up.
 //
 // Work split.  The flattened key space [B*H_kv][S] is cut into P contiguous
-// ranges of L keys, one CTA each (P ~ number of SMs), so every SM gets the
-// same number of keys whatever B, H_kv and S are.  A range can cross KV-head
-// boundaries; each piece (one head, keys [a, b)) is a "segment".  Pass-1
+// ranges of about L keys, one CTA each (P ~ number of SMs), so every SM gets
+// nearly the same number of keys whatever B, H_kv and S are; a range
+// boundary near a head boundary is moved onto it (range_begin).  A range can
+// cross KV-head boundaries; each piece (one head, keys [a, b)) is a
+// "segment".  Pass-1
 // partial normalisers and pass-2 candidate lists live in per-(CTA, segment)
 // slots whose number depends on P and B*H_kv only, never on S.
 //
@@ -93,8 +95,8 @@ __device__ __forceinline__ int p1_tile_order(int i, int ntiles) {
 // Segments of CTA c, in key order.
 __device__ __forceinline__ int cta_segments(const ScanArgs& A, int c, Seg* out) {
   const int64_t total = (int64_t)A.B * A.H_kv * A.S;
-  const int64_t f0 = (int64_t)c * A.L;
-  const int64_t f1 = min(f0 + A.L, total);
+  const int64_t f0 = range_begin(c, A.L, A.S, total);
+  const int64_t f1 = range_begin(c + 1, A.L, A.S, total);
   if (f0 >= f1) return 0;
   const int h0 = (int)(f0 / A.S), h1 = (int)((f1 - 1) / A.S);
   int n = 0;
@@ -115,12 +117,12 @@ __device__ __forceinline__ float2 merge_mz(float2 a, float2 b) {
 
 // (max, Z) of window row `row` of head bh over all pass-1 slots of the head.
 __device__ __forceinline__ float2 combine_partials(const ScanArgs& A, int bh, int row) {
-  const int64_t S = A.S;
-  const int c_first = (int)(((int64_t)bh * S) / A.L);
-  const int c_last = (int)((((int64_t)bh + 1) * S - 1) / A.L);
+  const int64_t S = A.S, total = (int64_t)A.B * A.H_kv * A.S;
+  const int c_first = (int)range_of((int64_t)bh * S, A.L, S, total);
+  const int c_last = (int)range_of(((int64_t)bh + 1) * S - 1, A.L, S, total);
   float2 st = make_float2(-INFINITY, 0.f);
   for (int c = c_first; c <= c_last; ++c) {
-    const int seg = bh - (int)(((int64_t)c * A.L) / S);
+    const int seg = bh - (int)(range_begin(c, A.L, S, total) / S);
     const size_t o = ((size_t)c * A.maxseg + seg) * A.gwp16 + row;
     st = merge_mz(st, make_float2(A.pm_in[o], A.pz_in[o]));
   }

@@ -39,12 +39,12 @@ struct SegView {
 // head starts inside it, so its slot is that CTA's first one.
 __device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int part) {
   const int64_t S = sp.S;
-  const int64_t c_first = ((int64_t)seg * S) / sp.L;
-  const int64_t c_last = (((int64_t)seg + 1) * S - 1) / sp.L;
+  const int64_t c_first = range_of((int64_t)seg * S, sp.L, S, sp.total);
+  const int64_t c_last = range_of(((int64_t)seg + 1) * S - 1, sp.L, S, sp.total);
   const int64_t c = c_first + part;
   if (c > c_last) return -1;
   if (part > 0) return c * sp.maxseg;
-  return c * sp.maxseg + (seg - (c * sp.L) / S);
+  return c * sp.maxseg + (seg - range_begin(c, sp.L, S, sp.total) / S);
 }
 
 // One thread-block cluster per (b, KV head).  The head's entries are cut
@@ -107,6 +107,7 @@ struct HeadView {
   const SelParams* sp;
   int seg;
   const int* pref;
+  const int64_t* slot_of;   // mode 1: candidate slot of each part (-1: none)
   int nparts;
   int stage_cap;   // entries of the share held in shared memory
 };
@@ -124,8 +125,7 @@ __device__ __forceinline__ uint64_t head_entry(const HeadView& hv, int f) {
     const int mid = (lo + hi + 1) >> 1;
     if (hv.pref[mid] <= f) lo = mid; else hi = mid - 1;
   }
-  const int64_t slot = cand_slot(*hv.sp, hv.seg, lo);
-  return hv.v->cand[(size_t)slot * hv.v->cap + (f - hv.pref[lo])];
+  return hv.v->cand[(size_t)hv.slot_of[lo] * hv.v->cap + (f - hv.pref[lo])];
 }
 
 // Entry f0 + i of this CTA's share (n entries).
@@ -273,7 +273,8 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
                   int* status) {
   extern __shared__ __align__(16) uint8_t cl_dyn[];
   uint64_t* stage = reinterpret_cast<uint64_t*>(cl_dyn);
-  int* pref = reinterpret_cast<int*>(cl_dyn + (size_t)stage_cap * sizeof(uint64_t));
+  int64_t* slot_of = reinterpret_cast<int64_t*>(cl_dyn + (size_t)stage_cap * sizeof(uint64_t));
+  int* pref = reinterpret_cast<int*>(slot_of + (v.mode == 0 ? 0 : sp.nparts));
   __shared__ ClSmem cs;
   const int seg = blockIdx.x / kCl;
   const int rank = (int)cluster_rank();
@@ -295,7 +296,9 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
       const int p = p0 + threadIdx.x;
       int len = 0;
       if (p < nparts) {
+        // each part's slot is worked out once here (it takes 64-bit divisions)
         const int64_t slot = cand_slot(sp, seg, p);
+        slot_of[p] = slot;
         len = slot < 0 ? 0 : min(max(v.cand_cnt[slot], 0), v.cap);
       }
       int tot;
@@ -306,7 +309,7 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
     E = carry;
   }
   __syncthreads();
-  HeadView hv{&v, &sp, seg, pref, nparts, stage_cap};
+  HeadView hv{&v, &sp, seg, pref, slot_of, nparts, stage_cap};
   const int f0 = (int)((int64_t)E * rank / kCl), f1 = (int)((int64_t)E * (rank + 1) / kCl);
   const int n = f1 - f0;
   const int mode = n_sel <= 0 ? 0 : n_sel >= E ? 2 : 1;
@@ -333,7 +336,7 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
         const int a = max(f0, pref[p]);
         const int e = min(f0 + ns, p + 1 < nparts ? pref[p + 1] : E);
         if (a >= e) continue;
-        const uint64_t* src = v.cand + (size_t)cand_slot(sp, seg, p) * v.cap - pref[p];
+        const uint64_t* src = v.cand + (size_t)slot_of[p] * v.cap - pref[p];
         // kCopyBatch independent loads in flight per thread
         for (int f = a + threadIdx.x; f < e; f += kCopyBatch * kClThreads) {
           uint64_t t[kCopyBatch];
@@ -518,7 +521,10 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   const int BH = B * sel.H_kv;
   cudaError_t e = cudaSuccess;
   const int np = mode == 0 ? 1 : sel.nparts;
-  auto smem_for = [np](int cap) { return (size_t)cap * sizeof(uint64_t) + (size_t)(np + 1) * sizeof(int); };
+  auto smem_for = [np, mode](int cap) {
+    return (size_t)cap * sizeof(uint64_t) + (mode == 0 ? 0 : (size_t)np * sizeof(int64_t)) +
+           (size_t)(np + 1) * sizeof(int);
+  };
   if (smem_for(kStageC) > 200 * 1024) return cudaErrorInvalidConfiguration;
   // the widest cluster that still gives every head its own CTAs in one wave;
   // 16 (two CTAs per SM, smaller shared-memory shares) only where the device
