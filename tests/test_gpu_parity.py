@@ -102,6 +102,40 @@ def test_candidate_compaction_path(K, ctas):
         U.check_head_outputs(k_out, v_out, pos, off, inp, cfg, 0, h, K_l_ref[h], o["s"], f"compaction ctas={ctas} h={h}")
 
 
+# (H_kv, S, scan CTAs) whose key-range boundaries land near head boundaries:
+# one snapped back onto a head start; one 76 keys past the snap distance (a
+# real two-segment CTA); one snapped forward at 232 keys next to a 234-key
+# near miss (the distance is 233); one forward and one back, both exactly at
+# the distance (140).
+SNAP_CASES = [(2, 700, 6), (2, 700, 9), (4, 700, 3), (4, 700, 5)]
+
+
+@pytest.mark.parametrize("H_kv,S,ctas", SNAP_CASES)
+def test_range_snapping_every_head(K, H_kv, S, ctas):
+    """Forced scan-CTA counts put range boundaries at and around the snap
+    distance from head boundaries; the compress path and the decomposed path
+    (whose pass-1 partials are merged per head by range) must both match the
+    oracle on every head."""
+    cfg = get_config("tiny", S=S, C=S, H_q=2 * H_kv, H_kv=H_kv, D=64, W=16, pool_k=5, K_l=150, recent=16,
+                     hh_frac=0.03, seed=50 + ctas)
+    inp = make_layer_inputs(cfg)
+    K_l, K_l_ref = U.kl_vector(cfg, K)
+    K.kvc_set_option(K.KVC_OPT_SCAN_CTAS, ctas)
+    try:
+        k_out, v_out, pos, off = U.run_compress(K, cfg, inp, K_l)
+        dec = U.run_decomposed(K, cfg, inp, K_l)
+    finally:
+        K.kvc_set_option(K.KVC_OPT_SCAN_CTAS, 0)
+    G = cfg.G
+    for h in range(cfg.H_kv):
+        o = U.oracle_head(cfg, inp, 0, h)
+        what = f"H_kv={H_kv} S={S} ctas={ctas} h={h}"
+        U.check_head_outputs(k_out, v_out, pos, off, inp, cfg, 0, h, K_l_ref[h], o["s"], what + " compress")
+        U.assert_mz_close(dec["m"][0, h * G:(h + 1) * G].reshape(-1), dec["Z"][0, h * G:(h + 1) * G].reshape(-1),
+                          o, what + " pass 1")
+        U.assert_scores_close(dec["scores"][0, h].numpy(), o["s"], cfg, what + " scores")
+
+
 def _select_case(K, S, H_kv, B, K_l, sink, recent, scores64):
     """GPU selection on given fp32 scores must equal the oracle's selection on
     the same fp32 values exactly (both decide in fp32)."""
