@@ -146,10 +146,7 @@ __device__ void cl_hist(const HeadView& hv, const uint64_t* stage, int f0, int n
     const int i = i0 + threadIdx.x;
     int bin = -1;
     if (i < n) bin = radix_bin((uint32_t)(share_entry(hv, stage, f0, n, i) >> 32), round, prefix);
-    // scores of one head share their leading bits, so many lanes hit the
-    // same digit: equal digits are merged into one shared-memory atomic
-    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-    if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+    if (bin >= 0) atomicAdd(&h[bin], 1u);
   }
 }
 
@@ -159,8 +156,7 @@ __device__ void cl_hist_surv(const uint32_t* surv, int ns, int round, uint32_t p
   for (int i0 = 0; i0 < ns; i0 += kClThreads) {
     const int i = i0 + threadIdx.x;
     const int bin = i < ns ? radix_bin(surv[i], round, prefix) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-    if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+    if (bin >= 0) atomicAdd(&h[bin], 1u);
   }
 }
 
