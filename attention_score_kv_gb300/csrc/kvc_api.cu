@@ -450,6 +450,15 @@ int kvc_compress_layer_deferred_v(int N, int layer, int B, int S, int C, int H_q
                         v_out, pos_out, ws, ws_bytes, reinterpret_cast<cudaEvent_t>(v_ready), stream);
 }
 
+int kvc_scan_ranges(int BH, int S, int P, int64_t* starts) {
+  if (BH < 1 || S < 1 || P < 1) return set_error(KVC_ERR_INVALID_ARG, "BH, S and P must be >= 1");
+  if (!starts) return set_error(KVC_ERR_INVALID_ARG, "starts must be non-NULL");
+  const ScanPlan pl = plan_for(BH, S, P);
+  const int64_t total = (int64_t)BH * S;
+  for (int c = 0; c <= pl.P; ++c) starts[c] = range_begin(c, pl.L, S, total);
+  return pl.P;
+}
+
 int kvc_retained_layout(int H_kv, int S, const int32_t* K_l, int64_t* out_off) {
   if (H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "H_kv and S must be >= 1");
   if (!K_l || !out_off) return set_error(KVC_ERR_INVALID_ARG, "K_l and out_off must be non-NULL");

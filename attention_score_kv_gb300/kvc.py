@@ -74,6 +74,7 @@ _SIGS = {
     "kvc_budget_inverse_stability_device": (_I, [_I, _I, _P, _I64, _I, _I, _P, _P]),
     "kvc_append_chunk": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_cache_layout": (_I, [_I, _I, _I, _I, _I32P, _I64P]),
+    "kvc_scan_ranges": (_I, [_I, _I, _I, _I64P]),
     "kvc_budget_pyramid": (_I, [_I, _I, _I, _I32P]),
     "kvc_retained_layout": (_I, [_I, _I, _I32P, _I64P]),
     "kvc_budget_inverse_stability": (_I, [_I, _F64P, _I64, _I, _I, _I32P]),
@@ -221,6 +222,15 @@ def kvc_compress_layer_deferred_v(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink,
                                               b_s, _ptr(q_win), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out),
                                               _ptr(pos_out), _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
                                               _event(v_ready), _stream(stream)))
+
+
+def kvc_scan_ranges(BH, S, P) -> list:
+    """Starts of the scan CTAs' key ranges over the flattened [BH][S] keys
+    when P CTAs are asked for (the last entry is BH * S)."""
+    out = (ctypes.c_int64 * (P + 1))()
+    n = _lib.kvc_scan_ranges(BH, S, P, out)
+    _check(min(n, 0))
+    return list(out[:n + 1])
 
 
 def kvc_retained_layout(H_kv, S, K_l) -> list:

@@ -301,6 +301,19 @@ int kvc_budget_pyramid(int N, int budget, int k_min, int32_t* K_l_out);
 int kvc_retained_layout(int H_kv, int S, const int32_t* K_l, int64_t* out_off);
 
 /*
+ * Host helper: the key ranges the two scans give their CTAs when P CTAs are
+ * asked for (the library asks for the SM count).  The flattened key space
+ * [BH][S] (BH = B * H_kv) is cut at c * L, L = ceil(BH*S / P), and a cut that
+ * lies within min(L/4, 512) keys of a head boundary is moved onto it, so no
+ * CTA spends a segment switch on a sliver of a head.
+ *   starts HOST [P + 1] out: range c is keys starts[c] .. starts[c+1]-1 of
+ *          the flattened space; starts[n] = BH * S.
+ * Returns n, the number of ranges (1 <= n <= P), or a negative code on
+ * invalid sizes (BH, S, P < 1) or a NULL pointer.  No device is touched.
+ */
+int kvc_scan_ranges(int BH, int S, int P, int64_t* starts);
+
+/*
  * Host helper (HeteroCache summary, Phase 2): per-KV-head budgets
  * proportional to w_h = 1 / s_h.  The exact shares total * w_h / sum(w) are
  * rounded by largest remainder (ties to the lower head index) so that they

@@ -166,3 +166,53 @@ def test_cache_layout_matches_oracle(K):
     from oracle import layer_major as LM
     K_l = [[100, 300, 9000], [64, 64, 64], [0, 1, 2]]
     assert K.kvc_cache_layout(3, 2, 3, 8192, K_l) == LM.cache_layout(3, 2, 8192, K_l).tolist()
+
+
+def _ranges_cases():
+    rng = np.random.default_rng(7)
+    cases = [(8, 131072, 152), (8, 65536, 152), (32, 32768, 152), (8, 8192, 152), (2, 700, 6), (2, 700, 9),
+             (4, 700, 3), (4, 700, 5), (1, 512, 152), (1, 1, 1), (3, 1000, 1), (16, 777, 152)]
+    for _ in range(200):
+        cases.append((int(rng.integers(1, 40)), int(rng.integers(1, 300000)), int(rng.integers(1, 200))))
+    return cases
+
+
+def test_scan_ranges_cover_the_keys_and_snap_to_heads(K):
+    """The CTA key ranges of the scans: ordered, non-empty, covering [0, BH*S)
+    exactly; a cut within min(L/4, 512) keys of a head boundary sits on it,
+    every other cut stays at c * L; a range is at most 2 * snap keys longer
+    than L and at least L / 2 long."""
+    for BH, S, P in _ranges_cases():
+        total = BH * S
+        st = K.kvc_scan_ranges(BH, S, P)
+        n = len(st) - 1
+        assert 1 <= n <= P
+        L = -(-total // min(P, total))
+        assert n == -(-total // L)
+        snap = min(L // 4, 512)
+        assert st[0] == 0 and st[-1] == total
+        for c in range(n):
+            assert st[c + 1] > st[c], (BH, S, P, c)
+            assert L // 2 <= st[c + 1] - st[c] <= L + 2 * snap or c == n - 1, (BH, S, P, c)
+        for c in range(1, n):
+            f, r = c * L, (c * L) % S
+            if r != 0 and (r <= snap or S - r <= snap):
+                assert st[c] % S == 0 and abs(st[c] - f) <= snap, (BH, S, P, c, st[c], f)
+            else:
+                assert st[c] == f, (BH, S, P, c, st[c], f)
+
+
+def test_scan_ranges_mistral_layer_has_no_two_head_range(K):
+    """Mistral-7B at S = 131072 on 152 CTAs: every range lies inside one KV
+    head (the unsnapped cut gave 7 CTAs a 9-63-key sliver of the next head)."""
+    S = 131072
+    st = K.kvc_scan_ranges(8, S, 152)
+    assert len(st) == 153
+    for a, b in zip(st[:-1], st[1:]):
+        assert a // S == (b - 1) // S
+
+
+def test_scan_ranges_rejects_bad_sizes(K):
+    for args in ((0, 10, 1), (1, 0, 1), (1, 10, 0)):
+        with pytest.raises(K.KvcError):
+            K.kvc_scan_ranges(*args)
