@@ -84,6 +84,28 @@ def test_compress_layer_rejects_bad_arguments(K, over, code):
     assert ei.value.code == code
 
 
+@pytest.mark.parametrize("over,code", [
+    (dict(H_q=5), -1),
+    (dict(layer=1), -1),
+    (dict(C=8), -1),
+    (dict(pool_k=4), -1),
+    (dict(v=0), -1),
+    (dict(k_out=0x4004), -1),
+    (dict(D=96), -2),
+])
+def test_deferred_v_rejects_bad_arguments_before_any_wait(K, over, code):
+    """kvc_compress_layer_deferred_v validates like kvc_compress_layer, on the
+    host, before it waits on the event or launches anything (the event
+    handle here is never touched)."""
+    a = dict(N=1, layer=0, B=1, S=512, C=512, H_q=4, H_kv=2, D=64, W=16, K_l=[128, 128], sink=4,
+             recent=16, pool_k=1, b_s=128, q_win=0x1000, k=0x2000, v=0x3000, k_out=0x4000,
+             v_out=0x5000, pos_out=0x6000, ws=0x10000, v_ready=0x7000, ws_bytes=1 << 30, stream=0)
+    a.update(over)
+    with pytest.raises(K.KvcError) as ei:
+        K.kvc_compress_layer_deferred_v(**a)
+    assert ei.value.code == code
+
+
 def test_budget_below_mandatory_set_is_rejected_before_launch(K):
     # |R_mand| = 4 + 16 = 20 > 19; checked on the host (no device needed to fail)
     with pytest.raises(K.KvcError) as ei:
