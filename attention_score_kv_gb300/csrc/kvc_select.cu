@@ -6,12 +6,11 @@
 // the values (the fused scorer's scores are >= 0 and keep their fp32 bits;
 // dense scores of either sign are mapped by flipping the sign bit of
 // positive values and all bits of negative ones); a three-round radix select
-// over those bits (11, 11
-// and 10 bits, each round a histogram of the keys that share the digits found
-// so far) finds the n_sel-th score T and how many keys scoring exactly T are
-// still needed.  Ties at T are taken in ascending index order, resolved with
-// per-warp counts and an ordered ballot write.  All of it runs in one launch
-// with one thread-block cluster per head.
+// over those bits (11, 11 and 10 bits, each round a histogram of the keys
+// that share the digits found so far) finds the n_sel-th score T and how many
+// keys scoring exactly T are still needed.  Ties at T are taken in ascending
+// index order, resolved with per-warp counts and an ordered ballot write.
+// All of it runs in one launch with one thread-block cluster per head.
 //
 // The keys come either from a dense score array (mode 0) or from the
 // per-range candidate lists of the fused scorer (mode 1, entries
@@ -51,9 +50,12 @@ __device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int p
 // into kCl contiguous shares, one per CTA, and each share is copied once
 // into that CTA's shared memory (up to stage_cap entries; the rest, if any, is
 // re-read from global memory in every round).  The radix rounds, the counts
-// and the ordered write then run on chip: per-CTA histograms are summed by
-// reading the other CTAs' shared memory, and hardware cluster barriers
-// separate the phases, so no CTA waits on anything outside its cluster.
+// and the ordered write then run on chip: per-CTA histograms (plain
+// shared-memory atomics) are summed by reading the other CTAs' shared
+// memory, and hardware cluster barriers separate the phases, so no CTA waits
+// on anything outside its cluster.  After the first round each CTA keeps
+// only the keys that share its digit (when they fit), so the later rounds
+// histogram those alone.
 constexpr int kMaxCl = 16;              // CTAs per head at most (a non-portable cluster size)
 constexpr int kClThreads = 512;
 constexpr int kClWarps = kClThreads / 32;
