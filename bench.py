@@ -45,9 +45,10 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["two_pass", "rawdot_int8"], default="two_pass",
+    ap.add_argument("--path", choices=["two_pass", "rawdot_int8", "append_chunk", "overlap"], default="two_pass",
                     help="two_pass: the layer compress (default, the headline); rawdot_int8: the single-pass "
-                         "INT8 raw inner-product scorer, then the same selection and gather")
+                         "INT8 raw inner-product scorer, then the same selection and gather; append_chunk: the "
+                         "layer-major chunk append; overlap: the HeteroCache overlap coefficient")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's S (smaller profiling captures); 0 keeps it")
     return ap.parse_args()
@@ -330,6 +331,108 @@ def run_rawdot(args):
     print(json.dumps(line), flush=True)
 
 
+def run_next_rows(args):
+    """Measurements of two "next" rows on one GPU: the layer-major chunk
+    append (one step = all C-key chunks of one layer's K and V appended to
+    the active buffers; bytes moved per second against the HBM peak) and the
+    HeteroCache overlap coefficient (one step = one call over 256 pairs of
+    4096-index sets; index bytes read per second).  One JSON line each."""
+    import numpy as np
+    import torch
+    from attention_score_kv_gb300 import build as _b
+    _b.build()
+    import attention_score_kv_gb300.kvc as K
+    from synth import make_layer_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, _, peak_kind = load_peaks()
+
+    def timed(fn, steps, warmup):
+        for i in range(max(3, warmup)):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        K.kvc_check_status(stream)
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.15)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        K.kvc_check_status(stream)
+        return e0.elapsed_time(e1) / steps, clk
+
+    if args.path == "append_chunk":
+        cfg = config_of(args)
+        nch = -(-cfg.S // cfg.C)
+        srcs = []
+        for layer_id in replica_layer_ids(0, min(args.layers, 2), cfg.N):
+            inp = make_layer_inputs(cfg, layer_id, device=dev)
+            srcs.append([(inp.k[:, :, j * cfg.C:(j + 1) * cfg.C].contiguous(),
+                          inp.v[:, :, j * cfg.C:(j + 1) * cfg.C].contiguous()) for j in range(nch)])
+            del inp
+        k_act = torch.empty((cfg.B, cfg.H_kv, cfg.S, cfg.D), dtype=torch.bfloat16, device=dev)
+        v_act = torch.empty_like(k_act)
+
+        def step(i):
+            for j, (kc, vc) in enumerate(srcs[i % len(srcs)]):
+                K.kvc_append_chunk(kc, vc, cfg.B, cfg.H_kv, cfg.S, cfg.C, cfg.D, j, k_act, v_act, stream=stream)
+
+        ms, clk = timed(step, args.steps, args.warmup)
+        moved = 2 * 2 * cfg.B * cfg.H_kv * cfg.S * cfg.D * 2      # K and V, read once and written once
+        gbs = moved / (ms / 1e3) / 1e9
+        line = {
+            "metric": "layer-major chunk append: bytes moved per second (K and V chunks into the active layer)",
+            "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(cfg), "path": f"append_chunk ({nch} chunks of C={cfg.C} per step)",
+                       "parallelism": "replicas x1", "l2": "each step moves 1.07 GB, far above L2"},
+            "roofline": {"bound": "hbm", "kernel": "append_chunk", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                         "alg_bytes_per_launch": moved / nch, "ms_per_launch": ms / nch},
+            "gpu_launches": nch * args.steps, "clocks": clk,
+        }
+    else:
+        rng = np.random.default_rng(5)
+        n_pairs, k_sel, S = 256, 4096, 131072
+
+        def sets():
+            out = []
+            for _ in range(n_pairs):
+                out.append(np.sort(rng.choice(S, k_sel, replace=False)).astype(np.int32))
+            return out
+        A, B = sets(), sets()
+        off = np.arange(n_pairs + 1, dtype=np.int64) * k_sel
+        a = torch.from_numpy(np.concatenate(A)).to(dev)
+        b = torch.from_numpy(np.concatenate(B)).to(dev)
+        a_off = torch.from_numpy(off).to(dev)
+        b_off = a_off.clone()
+        out = torch.empty(n_pairs, dtype=torch.float32, device=dev)
+        ms, clk = timed(lambda i: K.kvc_overlap_coefficient(a, a_off, b, b_off, n_pairs, out, stream=stream),
+                        args.steps, args.warmup)
+        read = 2 * n_pairs * k_sel * 4
+        gbs = read / (ms / 1e3) / 1e9
+        line = {
+            "metric": "HeteroCache overlap coefficient: index-set pairs per second",
+            "value": n_pairs / (ms / 1e3), "unit": "pairs/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": f"{n_pairs} pairs of ascending {k_sel}-index sets drawn from [0, {S})",
+                       "path": "overlap", "parallelism": "replicas x1", "l2": f"{read / 1e6:.1f} MB of indices (in L2)"},
+            "roofline": {"bound": "hbm", "kernel": "overlap", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                         "alg_bytes_per_launch": read, "ms_per_launch": ms},
+            "gpu_launches": args.steps, "clocks": clk,
+        }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -337,6 +440,9 @@ def main():
         return
     if args.path == "rawdot_int8":
         run_rawdot(args)
+        return
+    if args.path in ("append_chunk", "overlap"):
+        run_next_rows(args)
         return
     import torch
     import torch.distributed as dist
