@@ -34,7 +34,7 @@ METRIC = "layer-end compress: prefix keys scored/s per KV head; HBM GB/s vs ~8 T
 UNIT = "prefix keys scored/s (per KV head)"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
@@ -51,7 +51,7 @@ def parse():
                          "layer-major chunk append; overlap: the HeteroCache overlap coefficient")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="override the workload's S (smaller profiling captures); 0 keeps it")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def config_of(args):
