@@ -1,16 +1,22 @@
 // Pass 1 of the two-pass scorer (TideKV, Fig. 3): per window query, the
 // log-sum-exp normalisers over the prefix keys, kept as W-length state.
 //
-// A = window queries (two 128-row MMA blocks when G*W > 128), B = 128-key
-// tile.  The queries of a segment are copied once from shared into tensor
-// memory and feed every MMA of the segment from there, so the tensor core
-// reads only the key tile from shared memory.  Eight softmax warps read the
-// accumulators from tensor memory: with two blocks each thread owns one
-// query row and all 128 key columns of a tile; with one block the two warps
-// of a lane quarter split the columns.  Each thread keeps a reference
-// maximum m (raw dot-product units) and the sum Z of 2^(x - m * c),
-// x = q.k * c, c = log2(e)/sqrt(D), over its segment, then writes the
-// (m * c, Z) partial of its row to the segment's slot.
+// A = window queries (one or two 128-row MMA blocks), B = 128-key tile, both
+// read by the tensor core from shared memory; the accumulators rotate
+// through four 128-column tensor-memory buffers, one per (tile, query block)
+// "sub-tile".  Two threads on different warps issue the MMAs, taking
+// alternate sub-tiles: a thread that waits on an mbarrier stops feeding the
+// tensor core for a few hundred cycles, which a lone issuer of 64-cycle
+// MMAs cannot hide, while two issuers cover each other's waits.  Sixteen
+// softmax warps, four per tensor-memory lane quarter: with two query blocks,
+// warp k of a quarter reads block k/2, columns 64*(k%2) .. +63 of each tile;
+// with one block, columns 32*k .. +31.  A warp hands its buffer back as soon
+// as its columns are in registers, so the MMAs run ahead of the
+// exponentials by up to four sub-tiles.  Each thread owns one query row and
+// keeps a reference maximum m (raw dot-product units) and the sum Z of
+// 2^(x - m * c), x = q.k * c, c = log2(e)/sqrt(D), over its columns of the
+// segment; at the end of a segment the warps that share a row merge their
+// (m, Z) and write the row's (m * c, Z) partial to the segment's slot.
 #include "kvc_scan_common.cuh"
 
 namespace kvc {
@@ -18,41 +24,34 @@ namespace {
 
 using namespace scan;
 
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;
-
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiThreads) : "memory"); }
-
-// Tensor memory: three 128-column accumulator buffers, then the queries
-// (block mb, K-step ks at column kQCol + mb * D/2 + 8 * ks).  Accumulators
-// rotate through the buffers per (tile, 128-row query block) "sub-tile" u:
-// buffer u % 3, completed once per use, so the (u / 3)-th use of a buffer
-// waits on parity (u / 3) & 1.
-constexpr uint32_t kP1Bufs = 3;
-constexpr uint32_t kQCol = kP1Bufs * 128;
+constexpr int kSmxWarps = 16;
+constexpr int kSmxThreads = kSmxWarps * 32;
+constexpr int kFirstSmx = 3;                  // warp 0 TMA, warps 1-2 MMA issuers
+constexpr int kThreads = 32 * kFirstSmx + kSmxThreads;
+constexpr uint32_t kP1Bufs = 4;               // 128-column accumulator buffers
 constexpr float kBatchSumLimit = 1.152921504606846976e18f;   // 2^60
 
-__device__ __forceinline__ uint32_t p1_buf(uint32_t u) { return u % kP1Bufs; }
-__device__ __forceinline__ uint32_t p1_parity(uint32_t u) { return (u / kP1Bufs) & 1u; }
+__device__ __forceinline__ void smx_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kSmxThreads) : "memory"); }
 
-// Largest of 64 values (a tree, two chains).
-__device__ __forceinline__ float batch_max64(const float* v) {
+// Largest of N values (two chains).
+template <int N>
+__device__ __forceinline__ float batch_max(const float* v) {
   float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
 #pragma unroll
-  for (int c = 4; c < 64; c += 4) {
+  for (int c = 4; c < N; c += 4) {
     mx0 = fmaxf(mx0, fmaxf(v[c], v[c + 1]));
     mx1 = fmaxf(mx1, fmaxf(v[c + 2], v[c + 3]));
   }
   return fmaxf(mx0, mx1);
 }
 
-// Sum of 2^(v * c2 + nm) over 64 values, as two partial sums.
-__device__ __forceinline__ float2 batch_sum64(const float* v, float c2, float nm) {
+// Sum of 2^(v * c2 + nm) over N values, as two partial sums.
+template <int N>
+__device__ __forceinline__ float2 batch_sum(const float* v, float c2, float nm) {
   const float2 cc = make_float2(c2, c2), nn = make_float2(nm, nm);
   float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
-  for (int c = 0; c < 64; c += 8) {
+  for (int c = 0; c < N; c += 8) {
     const float2 x0 = __ffma2_rn(make_float2(v[c], v[c + 1]), cc, nn);
     const float2 x1 = __ffma2_rn(make_float2(v[c + 2], v[c + 3]), cc, nn);
     const float2 x2 = __ffma2_rn(make_float2(v[c + 4], v[c + 5]), cc, nn);
@@ -65,49 +64,48 @@ __device__ __forceinline__ float2 batch_sum64(const float* v, float c2, float nm
   return __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
 }
 
-template <int D>
-__device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, uint32_t adrain, const Seg* segs, int nseg,
-                          uint32_t sQ, uint32_t sK, uint32_t tmem, volatile int* abort_flag) {
+// MMA issuer `who` (0 or 1) of pass 1: sub-tiles u = NMB * tile + block with
+// u % 2 == who, in order.  A tile's ring stage is released by a commit of
+// each issuer that used it; the queries of a segment, by a commit of both.
+template <int D, int NMB>
+__device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, const Seg* segs, int nseg, uint32_t sQ, uint32_t sK,
+                          uint32_t tmem, int who, volatile int* abort_flag) {
   constexpr int NKH = D / 64;
   constexpr int KSTEPS = D / 16;
   constexpr uint32_t kTileBytes = kTile * 128 * NKH;
   const uint32_t q_half = (uint32_t)A.nq * 128;
   const uint32_t idesc = tc::idesc_bf16(128, 128);
-  const uint32_t tq = tmem + kQCol;
-  uint32_t stage = 0, phase = 0, qphase = 0, u = 0;
+  uint32_t qphase = 0, u = 0, tcount = 0;
   for (int si = 0; si < nseg; ++si) {
     const Seg sg = segs[si];
     if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) return;
     qphase ^= 1;
-    // the previous segment's MMAs must be done reading the old queries
-    if (si > 0 && !wait_bar(adrain, (uint32_t)(si - 1) & 1u, abort_flag, A.status)) return;
-    tc::fence_after_sync();
-    for (int mb = 0; mb < A.n_mb; ++mb)
-#pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        const uint32_t qoff = (ks >> 2) * q_half + mb * (128 * 128) + (ks & 3) * 32;
-        tc::tmem_cp_128x256b(tq + mb * (D / 2) + ks * 8, tc::desc_sw128(sQ + qoff));
-      }
-    tc::mma_commit(smem_u32(&bars->qempty));   // shared-memory queries free once copied
     const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
-    for (int t = 0; t < ntiles; ++t) {
-      if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status)) return;
-      const uint32_t kb = sK + stage * kTileBytes;
-      for (int mb = 0; mb < A.n_mb; ++mb, ++u) {
-        const uint32_t b = p1_buf(u);
-        if (!wait_bar(smem_u32(&bars->tempty[b]), p1_parity(u) ^ 1u, abort_flag, A.status)) return;
+    for (int t = 0; t < ntiles; ++t, ++tcount) {
+      const uint32_t stage = tcount % kStages, phase = (tcount / kStages) & 1u;
+      bool mine = false;
+      for (int mb = 0; mb < NMB; ++mb, ++u) {
+        if ((int)(u & 1u) != who) continue;
+        if (!mine) {
+          if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status)) return;
+          mine = true;
+        }
+        const uint32_t b = u % kP1Bufs;
+        if (!wait_bar(smem_u32(&bars->tempty[b]), ((u / kP1Bufs) & 1u) ^ 1u, abort_flag, A.status)) return;
         tc::fence_after_sync();
+        const uint32_t kb = sK + stage * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
           const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
-          tc::mma_bf16_ta(tmem + b * 128, tq + mb * (D / 2) + ks * 8, tc::desc_sw128(kb + koff), idesc, ks > 0);
+          const uint32_t qoff = (ks >> 2) * q_half + mb * (128 * 128) + (ks & 3) * 32;
+          tc::mma_bf16(tmem + b * 128, tc::desc_sw128(sQ + qoff), tc::desc_sw128(kb + koff), idesc, ks > 0);
         }
         tc::mma_commit(smem_u32(&bars->tfull[b]));
       }
-      tc::mma_commit(smem_u32(&bars->empty[stage]));
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
+      if (mine) tc::mma_commit(smem_u32(&bars->empty[stage]));
     }
-    if (si + 1 < nseg) tc::mma_commit(adrain);
+    // the queries in shared memory are free once this segment's MMAs are done
+    tc::mma_commit(smem_u32(&bars->qempty));
   }
 }
 
@@ -115,23 +113,22 @@ template <int D, int NMB, bool EXACT_MAX>
 __global__ void __launch_bounds__(kThreads, 1)
 kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap) {
-  constexpr int NKH = D / 64;
-  constexpr int NC = NMB == 2 ? 128 : 64;       // accumulator columns per softmax thread
+  constexpr int NCW = NMB == 2 ? 64 : 32;       // accumulator columns per softmax warp per tile
+  constexpr int NPART = NMB == 2 ? 2 : 4;       // warps sharing a query row
   extern __shared__ uint8_t smem_raw[];
   __shared__ PipeBars bars;
-  __shared__ uint64_t adrain;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ float2 s_half[128];
+  __shared__ float2 s_part[4][128];
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = base;
-  const uint32_t sK = base + (uint32_t)A.nq * 128 * NKH;
+  const uint32_t sK = base + (uint32_t)A.nq * 128 * (D / 64);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    init_pipe_bars(&bars, NMB == 2 ? kEpiWarps / 2 : kEpiWarps);
-    tc::mbar_init(smem_u32(&adrain), 1);
+    // a stage is used by both issuers with two query blocks, by one otherwise
+    init_pipe_bars(&bars, kSmxWarps / NMB, kStages, NMB, 2);
     s_abort = 0;
     tc::fence_barrier_init();
   }
@@ -153,21 +150,18 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       tc::tma_prefetch_desc(&kmap);
       producer<D, 1>(A, &qmap, &kmap, &bars, sQ, sK, &s_abort);
     }
-  } else if (warp == 1) {
+  } else if (warp < kFirstSmx) {
     if (lane == 0) {
       Seg segs[kMaxSegs];
       const int nseg = cta_segments(A, blockIdx.x, segs);
-      mma_pass1<D>(A, &bars, smem_u32(&adrain), segs, nseg, sQ, sK, tmem, &s_abort);
+      mma_pass1<D, NMB>(A, &bars, segs, nseg, sQ, sK, tmem, warp - 1, &s_abort);
     }
   } else {
-    // Softmax warps: with two query blocks the four warps of group k read
-    // block k (each thread one query row, all 128 key columns of a tile);
-    // with one block the two warps of a lane quarter split the columns.
-    const int e = warp - 2;
+    const int k = (warp - kFirstSmx) >> 2;     // 0..3
     const int quarter = warp & 3;              // TMEM lanes this warp may read
-    const int k = e >> 2;                      // 0 or 1
-    const int mb = NMB == 2 ? k : 0;
-    const int col0 = NMB == 2 ? 0 : 64 * k;
+    const int mb = NMB == 2 ? (k >> 1) : 0;
+    const int part = NMB == 2 ? (k & 1) : k;   // column slice of the tile
+    const int col0 = part * NCW;
     const int row = mb * 128 + quarter * 32 + lane;
     const bool active = (mb * 128 + quarter * 32) < A.gw;
     const float c2 = A.c2;
@@ -185,86 +179,75 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
       for (int ti = 0; ti < ntiles && ok; ++ti, ++tcount) {
         const int t = p1_tile_order(ti, ntiles);
-        const uint32_t u = NMB == 2 ? 2 * tcount + mb : tcount;   // this warp's sub-tile
-        const uint32_t buf = p1_buf(u);
-        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), p1_parity(u), &s_abort, A.status)) { ok = false; break; }
+        const uint32_t u = (uint32_t)NMB * tcount + (uint32_t)mb;   // this warp's sub-tile
+        const uint32_t buf = u % kP1Bufs;
+        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), (u / kP1Bufs) & 1u, &s_abort, A.status)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t taddr = tmem + buf * 128 + col0 + ((uint32_t)(quarter * 32) << 16);
-        // 64 accumulator columns at a time; the buffer is handed back to the
-        // MMA warp right after the last batch has been read.  Every warp
-        // loads, active or not (a load under a runtime condition costs far
-        // more than the rows an idle warp never uses).
-#pragma unroll 1
-        for (int bt = 0; bt < NC / 64; ++bt) {
-          float v[64];
+        // Every warp loads, active or not (a load under a runtime condition
+        // costs far more than the rows an idle warp never uses); the buffer
+        // goes back to the MMA warp right after.
+        float v[NCW];
 #pragma unroll
-          for (int c = 0; c < 64; c += 16) tc::tmem_ld16(taddr + bt * 64 + c, v + c);
-          tc::tmem_wait_ld();
-          tc::reg_fence(v, 64);
-          if (bt == NC / 64 - 1) {
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[buf]));
-          }
-          if (!active) continue;
-          const int t0 = sg.a + t * kTile + col0 + bt * 64;
-          if (t0 + 63 >= sg.b || t0 + 63 > A.S - A.W) {
+        for (int c = 0; c < NCW; c += 16) tc::tmem_ld16(taddr + c, v + c);
+        tc::tmem_wait_ld();
+        tc::reg_fence(v, NCW);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[buf]));
+        if (!active) continue;
+        const int t0 = sg.a + t * kTile + col0;
+        if (t0 + NCW - 1 >= sg.b || t0 + NCW - 1 > A.S - A.W) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const int j = t0 + c;
-              if (j >= sg.b || j > t_row) v[c] = -INFINITY;
-            }
-          }
-          if (EXACT_MAX) {
-            // running maximum: the sum so far is rescaled when it grows
-            const float mx = batch_max64(v);
-            if (mx > mref) {
-              const float sc = (mref == -INFINITY) ? 0.f : ex2((mref - mx) * c2);
-              z2.x *= sc;
-              z2.y *= sc;
-              mref = mx;
-            }
-            if (mref > -INFINITY) z2 = __fadd2_rn(z2, batch_sum64(v, c2, -mref * c2));
-            continue;
-          }
-          // The sum is kept relative to a reference mref (raw units): the
-          // first finite batch maximum of the segment.  A batch whose sum
-          // passes 2^60 (a score far above mref) is redone against a raised
-          // reference, so the fp32 state never overflows; any reference gives
-          // the same log-sum-exp.
-          if (mref == -INFINITY) mref = batch_max64(v);
-          if (mref > -INFINITY) {
-            float2 bs = batch_sum64(v, c2, -mref * c2);
-            if (!(bs.x + bs.y <= kBatchSumLimit)) {
-              const float mnew = fmaxf(mref, batch_max64(v));
-              const float sc = ex2((mref - mnew) * c2);
-              z2.x *= sc;
-              z2.y *= sc;
-              mref = mnew;
-              bs = batch_sum64(v, c2, -mref * c2);
-            }
-            z2 = __fadd2_rn(z2, bs);
+          for (int c = 0; c < NCW; ++c) {
+            const int j = t0 + c;
+            if (j >= sg.b || j > t_row) v[c] = -INFINITY;
           }
         }
+        if (EXACT_MAX) {
+          // running maximum: the sum so far is rescaled when it grows
+          const float mx = batch_max<NCW>(v);
+          if (mx > mref) {
+            const float sc = (mref == -INFINITY) ? 0.f : ex2((mref - mx) * c2);
+            z2.x *= sc;
+            z2.y *= sc;
+            mref = mx;
+          }
+          if (mref > -INFINITY) z2 = __fadd2_rn(z2, batch_sum<NCW>(v, c2, -mref * c2));
+          continue;
+        }
+        // The sum is kept relative to a reference mref (raw units): the
+        // first finite batch maximum of the segment.  A batch whose sum
+        // passes 2^60 (a score far above mref) is redone against a raised
+        // reference, so the fp32 state never overflows; any reference gives
+        // the same log-sum-exp.
+        if (mref == -INFINITY) mref = batch_max<NCW>(v);
+        if (mref > -INFINITY) {
+          float2 bs = batch_sum<NCW>(v, c2, -mref * c2);
+          if (!(bs.x + bs.y <= kBatchSumLimit)) {
+            const float mnew = fmaxf(mref, batch_max<NCW>(v));
+            const float sc = ex2((mref - mnew) * c2);
+            z2.x *= sc;
+            z2.y *= sc;
+            mref = mnew;
+            bs = batch_sum<NCW>(v, c2, -mref * c2);
+          }
+          z2 = __fadd2_rn(z2, bs);
+        }
       }
-      // segment done: the two column halves of a row (one block) are merged
+      // segment done: the NPART column slices of a row are merged in slice order
       const float2 mine = make_float2(mref == -INFINITY ? -INFINITY : mref * c2, z2.x + z2.y);
       const size_t slot = (size_t)blockIdx.x * A.maxseg + (size_t)(sg.bh - segs[0].bh);
-      if (NMB == 2) {
-        if (ok && row < A.gwp16) {
-          A.part_m[slot * A.gwp16 + row] = mine.x;
-          A.part_z[slot * A.gwp16 + row] = mine.y;
-        }
-      } else {
-        if (k == 1) s_half[quarter * 32 + lane] = mine;
-        epi_sync();
-        if (ok && k == 0 && row < A.gwp16) {
-          const float2 st = merge_mz(mine, s_half[quarter * 32 + lane]);
-          A.part_m[slot * A.gwp16 + row] = st.x;
-          A.part_z[slot * A.gwp16 + row] = st.y;
-        }
-        epi_sync();
+      s_part[k][quarter * 32 + lane] = mine;
+      smx_sync();
+      if (part == 0 && ok && row < A.gwp16) {
+        float2 st = mine;
+#pragma unroll
+        for (int q = 1; q < NPART; ++q) st = merge_mz(st, s_part[k + q][quarter * 32 + lane]);
+        A.part_m[slot * A.gwp16 + row] = st.x;
+        A.part_z[slot * A.gwp16 + row] = st.y;
       }
+      smx_sync();
     }
   }
   tc::fence_before_sync();

@@ -11,13 +11,16 @@
 // (hi, mid, lo) on the query side, so the accumulator already holds
 // q.k - lse_q in raw units and a weight is 2^(acc * log2(e)/sqrt(D)).
 //
-// Two groups of four softmax warps take alternate tiles (group g reads
-// accumulator buffer g); each thread owns one key and sums its weights over
-// every column in registers, then hands the key's mass r_j to a shared-memory
-// ring.  A pooling warp consumes the ring in key order: it keeps the last
-// pool_k-1 masses of the previous tile, forms the centred average for keys
-// t0 - h .. t0 + 127 - h, and appends the non-mandatory keys that beat the
-// range's running threshold.
+// Sixteen softmax warps, four per tensor-memory lane quarter, share every
+// tile: warp k of a quarter reads column slice k of the accumulator once
+// (up to 64 columns), hands the buffer back to the MMA warp at once, then
+// exponentiates and sums its columns in registers.  So the MMA of the next
+// tiles never waits on the exponentials, only on the loads.  Each thread
+// owns one key; the four slice sums of a key go to a shared-memory ring.  A
+// pooling warp consumes the ring in key order: it adds the four slices, keeps
+// the last pool_k-1 masses of the previous tile, forms the centred average
+// for keys t0 - h .. t0 + 127 - h, and appends the non-mandatory keys that
+// beat the range's running threshold.
 #include "kvc_scan_common.cuh"
 
 namespace kvc {
@@ -26,8 +29,9 @@ namespace {
 using namespace scan;
 
 constexpr int kStages2 = 3;
-constexpr int kGroupWarps = 4;                   // one warp per TMEM lane quarter
-constexpr int kPoolWarp = 2 + 2 * kGroupWarps;   // warp 10
+constexpr int kSmxWarps = 16;                    // four per TMEM lane quarter
+constexpr int kSlices = kSmxWarps / 4;           // column slices of a tile
+constexpr int kPoolWarp = 2 + kSmxWarps;         // warp 18
 constexpr int kThreads = 32 * (kPoolWarp + 1);
 constexpr int kRing = 4;
 constexpr int kRingPad = 16;                     // room for the previous tile's last 2h masses
@@ -231,7 +235,8 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
   __shared__ RingBars rbars;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ float s_ring[kRing][kRingPad + kTile];
+  __shared__ __align__(16) float s_ring[kRing][kRingPad + kTile];   // key masses, pooled in key order
+  __shared__ __align__(16) float s_part[kRing][kSlices][kTile];     // per-slice sums of each key
   __shared__ WarpCompact s_wc;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -242,9 +247,9 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    init_pipe_bars(&bars, kGroupWarps, kStages2);
+    init_pipe_bars(&bars, kSmxWarps, kStages2);
     for (int i = 0; i < kRing; ++i) {
-      tc::mbar_init(smem_u32(&rbars.rfull[i]), kGroupWarps * 32);
+      tc::mbar_init(smem_u32(&rbars.rfull[i]), kSmxWarps);
       tc::mbar_init(smem_u32(&rbars.rempty[i]), 1);
     }
     tc::mbar_init(smem_u32(&rbars.bias_free), 1);
@@ -279,93 +284,92 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
     mma_warp<D>(A, &bars, &rbars, segs, nseg, sQ, sK, sOnes, sBias, tmem, &s_abort);
   } else if (warp < kPoolWarp) {
     // ---------------------------------------------------- softmax warps
-    const int g = (warp - 2) / kGroupWarps;
+    // Warp k of a lane quarter owns column chunks [k*cw, k*cw + cw) of the
+    // G*W (rounded to 16) window columns, cw = ceil(chunks / 4) <= 4.  It
+    // always loads four 16-column chunks (they stay inside the 256-column
+    // buffer); chunks past its slice or past the last one weigh nothing.
+    const int k = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int krow = quarter * 32 + lane;
     const int nch = A.gwp16 / 16;
-    const int nbt = (nch + 3) / 4;
+    const int cw = (nch + kSlices - 1) / kSlices;
+    const int c0 = k * cw;
+    const int c_end = min(c0 + cw, nch);     // chunks c0 .. c_end-1 are this warp's
     const float c2 = A.c2;
     const float2 cc = make_float2(c2, c2);
-    const uint32_t taddr = tmem + g * kAccStride + ((uint32_t)(quarter * 32) << 16);
-    uint32_t tph = 0;
+    const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
     int tcount = 0;
     bool ok = true;
     for (int s = 0; s < nseg && ok; ++s) {
       const Seg sg = segs[s];
       const int n_iter = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
       for (int it = 0; it < n_iter; ++it, ++tcount) {
-        if ((tcount & 1) != g) continue;
         const int t0 = sg.a - hw + it * kTile;
-        if (!wait_bar_warp(smem_u32(&bars.tfull[g]), tph, &s_abort, A.status)) { ok = false; break; }
-        tph ^= 1;
+        const uint32_t buf = (uint32_t)tcount & 1u;
+        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), ((uint32_t)tcount >> 1) & 1u, &s_abort, A.status)) {
+          ok = false;
+          break;
+        }
         tc::fence_after_sync();
+        float v[64];
+        const uint32_t taddr = tmem + buf * kAccStride + tlane + (uint32_t)c0 * 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tc::tmem_ld16(taddr + i * 16, v + 16 * i);
+        tc::tmem_wait_ld();
+        tc::reg_fence(v, 64);
+        // the accumulator is free for the MMA warp as soon as it is in registers
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[buf]));
         const int j = t0 + krow;
         const bool need_mask = (t0 + kTile - 1 > A.S - A.W);
         float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-#pragma unroll 1
-        for (int bt = 0; bt < nbt; ++bt) {
-          // all four column chunks are loaded even past the last one in use
-          // (they stay inside this group's 256-column buffer): a load under a
-          // runtime condition costs far more than the unused columns
-          float v[64];
+        if (!need_mask) {
+          if (c0 + 4 > c_end) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) tc::tmem_ld16(taddr + (4 * bt + i) * 16, v + 16 * i);
-          tc::tmem_wait_ld();
-          tc::reg_fence(v, 64);
-          if (bt == nbt - 1) {
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[g]));
+            for (int i = 0; i < 4; ++i)
+              if (c0 + i >= c_end) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[16 * i + q] = -INFINITY;
+              }
           }
-          if (!need_mask) {
-            // a ragged last batch: its unused columns weigh 2^-inf = 0, so
-            // the 64 columns below run as one unguarded block
-            if (4 * bt + 4 > nch) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (4 * bt + i >= nch) {
+          for (int c = 0; c < 64; c += 8) {
+            const float2 x0 = __fmul2_rn(make_float2(v[c], v[c + 1]), cc);
+            const float2 x1 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), cc);
+            const float2 x2 = __fmul2_rn(make_float2(v[c + 4], v[c + 5]), cc);
+            const float2 x3 = __fmul2_rn(make_float2(v[c + 6], v[c + 7]), cc);
+            a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
+            a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
+            a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
+            a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+          }
+        } else {
+          // tiles near the window: window query i (column g*W + i) sees key
+          // j only when j <= S - W + i, i.e. i >= dj
+          const int dj = j - (A.S - A.W);
 #pragma unroll
-                  for (int q = 0; q < 16; ++q) v[16 * i + q] = -INFINITY;
-                }
-            }
+          for (int i = 0; i < 4; ++i) {
+            if (c0 + i < c_end) {
+              int wi = ((c0 + i) * 16) % A.W;
 #pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-              const float2 x0 = __fmul2_rn(make_float2(v[c], v[c + 1]), cc);
-              const float2 x1 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), cc);
-              const float2 x2 = __fmul2_rn(make_float2(v[c + 4], v[c + 5]), cc);
-              const float2 x3 = __fmul2_rn(make_float2(v[c + 6], v[c + 7]), cc);
-              a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
-              a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
-              a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
-              a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
-            }
-          } else {
-            // tiles near the window: window query i (column g*W + i) sees key
-            // j only when j <= S - W + i, i.e. i >= dj
-            const int dj = j - (A.S - A.W);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (4 * bt + i < nch) {
-                int wi = ((4 * bt + i) * 16) % A.W;
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                  const float e = ex2(v[16 * i + q] * c2);
-                  a0.x += wi >= dj ? e : 0.f;
-                  if (++wi == A.W) wi = 0;
-                }
+              for (int q = 0; q < 16; ++q) {
+                const float e = ex2(v[16 * i + q] * c2);
+                a0.x += wi >= dj ? e : 0.f;
+                if (++wi == A.W) wi = 0;
               }
             }
           }
         }
-        float r = (a0.x + a0.y) + (a1.x + a1.y) + ((a2.x + a2.y) + (a3.x + a3.y));
-        if (j < 0 || j >= A.S) r = 0.f;
+        const float r = (a0.x + a0.y) + (a1.x + a1.y) + ((a2.x + a2.y) + (a3.x + a3.y));
         const int slot = tcount % kRing;
         if (!wait_bar_warp(smem_u32(&rbars.rempty[slot]), ((tcount / kRing) & 1) ^ 1, &s_abort, A.status)) {
           ok = false;
           break;
         }
-        s_ring[slot][kRingPad + krow] = r;
-        tc::mbar_arrive(smem_u32(&rbars.rfull[slot]));
+        s_part[slot][k][krow] = r;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(smem_u32(&rbars.rfull[slot]));
       }
     }
   } else {
@@ -391,21 +395,58 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
           __syncwarp();
         }
         if (!wait_bar_warp(smem_u32(&rbars.rfull[slot]), (tcount / kRing) & 1, &s_abort, A.status)) { ok = false; break; }
-        // lane l pools keys t0 - h + 4l + k, k = 0..3, over masses win[k .. k + 2h]:
-        // the 4 + 2h masses are loaded into registers first, then summed in
-        // ascending order, so no add waits on a shared-memory load
-        const float* win = rr + kRingPad - 2 * hw + 4 * lane;
-        float wv[4 + kRingPad];
+        {
+          // key mass = the sum of its four slice sums; keys outside [0, S) weigh nothing
+          const int jb = t0 + 4 * lane;
+          float4 m4 = *reinterpret_cast<const float4*>(&s_part[slot][0][4 * lane]);
 #pragma unroll
-        for (int i = 0; i < 4 + kRingPad; ++i) wv[i] = (i < 4 + 2 * hw) ? win[i] : 0.f;
+          for (int q = 1; q < kSlices; ++q) {
+            const float4 p4 = *reinterpret_cast<const float4*>(&s_part[slot][q][4 * lane]);
+            m4.x += p4.x;
+            m4.y += p4.y;
+            m4.z += p4.z;
+            m4.w += p4.w;
+          }
+          if (jb < 0 || jb + 3 >= A.S) {
+            if (jb + 0 < 0 || jb + 0 >= A.S) m4.x = 0.f;
+            if (jb + 1 < 0 || jb + 1 >= A.S) m4.y = 0.f;
+            if (jb + 2 < 0 || jb + 2 >= A.S) m4.z = 0.f;
+            if (jb + 3 < 0 || jb + 3 >= A.S) m4.w = 0.f;
+          }
+          *reinterpret_cast<float4*>(&rr[kRingPad + 4 * lane]) = m4;
+          __syncwarp();
+        }
+        // lane l pools keys t0 - h + 4l + k, k = 0..3, over the masses of keys
+        // t0 - 2h + 4l + k .. t0 + 4l + k, summed in ascending key order
         float sc[4];
+        if (hw == 3) {
+          // the 7-wide pool of the long-context workloads: three aligned
+          // 16-byte loads cover the ten masses a lane needs
+          const float* b4 = rr + kRingPad - 8 + 4 * lane;
+          const float4 x0 = *reinterpret_cast<const float4*>(b4);
+          const float4 x1 = *reinterpret_cast<const float4*>(b4 + 4);
+          const float4 x2 = *reinterpret_cast<const float4*>(b4 + 8);
+          const float w[12] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, x2.x, x2.y, x2.z, x2.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float acc = 0.f;
+          for (int k = 0; k < 4; ++k) {
+            float acc = w[2 + k];
 #pragma unroll
-          for (int d = 0; d <= kRingPad; ++d)
-            if (d <= 2 * hw) acc += wv[k + d];
-          sc[k] = A.pool_k == 1 ? acc : acc * inv_pool;
+            for (int d = 1; d <= 6; ++d) acc += w[2 + k + d];
+            sc[k] = acc * inv_pool;
+          }
+        } else {
+          const float* win = rr + kRingPad - 2 * hw + 4 * lane;
+          float wv[4 + kRingPad];
+#pragma unroll
+          for (int i = 0; i < 4 + kRingPad; ++i) wv[i] = (i < 4 + 2 * hw) ? win[i] : 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float acc = 0.f;
+#pragma unroll
+            for (int d = 0; d <= kRingPad; ++d)
+              if (d <= 2 * hw) acc += wv[k + d];
+            sc[k] = A.pool_k == 1 ? acc : acc * inv_pool;
+          }
         }
         const int j0 = t0 - hw + 4 * lane;
         if (!CAND) {
@@ -422,17 +463,20 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
             const int jo = j0 + k;
             is_cand[k] = jo >= sg.a && jo < sg.b && jo >= sel.r_lo && jo < sel.r_hi;
           }
+          // a key's place in the list: the candidates of lower lanes first,
+          // then this lane's lower keys (four ballots, no scan)
+          const unsigned lt = (1u << lane) - 1u;
           for (int tries = 0;; ++tries) {
-            int n_mine = 0;
+            bool take[4];
+            unsigned bal[4];
+            int before = 0, n_new = 0;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) n_mine += (is_cand[k] && (long long)u[k] > tau) ? 1 : 0;
-            int incl = n_mine;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const int t = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += t;
+            for (int k = 0; k < 4; ++k) {
+              take[k] = is_cand[k] && (long long)u[k] > tau;
+              bal[k] = __ballot_sync(0xffffffffu, take[k]);
+              before += __popc(bal[k] & lt);
+              n_new += __popc(bal[k]);
             }
-            const int n_new = __shfl_sync(0xffffffffu, incl, 31);
             if (cnt + n_new > A.cap) {
               if (cnt <= n_keep || tries >= 2) {
                 if (lane == 0) record_status(A.status, kStatusCandOverflow);
@@ -441,12 +485,10 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
               cnt = warp_compact(my_cand, cnt, n_keep, &s_wc, &tau, A.status);
               continue;
             }
-            int pos = cnt + incl - n_mine;
+            int pos = cnt + before;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              if (is_cand[k] && (long long)u[k] > tau) {
-                my_cand[pos++] = ((uint64_t)u[k] << 32) | (uint32_t)(j0 + k);
-              }
+              if (take[k]) my_cand[pos++] = ((uint64_t)u[k] << 32) | (uint32_t)(j0 + k);
             }
             cnt += n_new;
             break;

@@ -12,9 +12,8 @@
 // slots whose number depends on P and B*H_kv only, never on S.
 //
 // Warp 0 issues TMA loads (the group's window queries once per segment, then
-// 128-key tiles through a 4-stage ring), warp 1 owns tensor memory and issues
-// the MMAs from one thread into two 256-column accumulator buffers, so the
-// MMA of tile t+1 runs while tile t is being reduced.  Every mbarrier wait is
+// 128-key tiles through a shared-memory ring); the MMA warps and the softmax
+// warps of each scan are described in its own file.  Every mbarrier wait is
 // bounded; a wait that gives up records a timeout in the status word and the
 // CTA drains and returns.
 #pragma once
@@ -75,13 +74,19 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return false;
 }
 
-// Bounded wait by a whole warp: only lane 0 polls the barrier (many threads
-// spinning on one mbarrier word slow down the shared-memory traffic of the
-// TMA and the MMAs), then the warp is released together.
+// Bounded wait by a whole warp.  Every lane reads the barrier in the same
+// instruction, so the warp never diverges: a barrier that is already
+// complete costs one read (about 20 cycles), where one polling lane plus a
+// broadcast costs over 300 (the warp splits and reconverges around the poll).
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 4095u) == 4095u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  if ((threadIdx.x & 31) == 0) record_status(status, kStatusTimeout);
+  return false;
 }
 
 // Pass-1 tile order within a segment: the leading third of the keys comes
@@ -133,17 +138,20 @@ struct PipeBars {
   uint64_t full[kMaxStages], empty[kMaxStages], tfull[4], tempty[4], qfull, qempty;
 };
 
-__device__ __forceinline__ void init_pipe_bars(PipeBars* b, int tempty_count, int nst = kStages) {
+// empty_count / qempty_count: commits that free a ring stage / the queries
+// (one per MMA-issuing thread that used them).
+__device__ __forceinline__ void init_pipe_bars(PipeBars* b, int tempty_count, int nst = kStages, int empty_count = 1,
+                                               int qempty_count = 1) {
   for (int i = 0; i < nst; ++i) {
     tc::mbar_init(smem_u32(&b->full[i]), 1);
-    tc::mbar_init(smem_u32(&b->empty[i]), 1);
+    tc::mbar_init(smem_u32(&b->empty[i]), empty_count);
   }
   for (int i = 0; i < 4; ++i) {
     tc::mbar_init(smem_u32(&b->tfull[i]), 1);
     tc::mbar_init(smem_u32(&b->tempty[i]), tempty_count);
   }
   tc::mbar_init(smem_u32(&b->qfull), 1);
-  tc::mbar_init(smem_u32(&b->qempty), 1);
+  tc::mbar_init(smem_u32(&b->qempty), qempty_count);
 }
 
 // TMA producer (one thread): per segment the window queries, then the key
