@@ -36,21 +36,24 @@ Functions and their pins (tests/test_oracle_pins.py):
   avg_pool: brute force, hand example, k=1 identity, np.convolve.
   mandatory_set, select_topk: brute force, raw-dot-product special case,
       all-equal ties, |kept| = min(K_l, S), R_mand kept.
-  gather: identity on the selected rows.
+  gather: position-encoding rows (golden), order and off-by-one.
+  group_queries: hand-built GQA case whose scores follow from the head map.
   two_pass_blockwise: equals the dense path; temp independent of S.
-  budgets_inverse_stability: sums, proportionality, clamps.
+  budgets_inverse_stability: exact-rational shares; sums, proportionality,
+      clamps, a hand-worked largest-remainder case.
   retained_cache_bytes: 512 MiB at TideKV's main setting.
 """
 
 from __future__ import annotations
 
 import math
+from fractions import Fraction
 
 import numpy as np
 
 __all__ = [
     "as_f64", "window_positions", "dense_logits", "lse_normalisers",
-    "attention_weights", "window_group_sum", "avg_pool", "score_head",
+    "attention_weights", "window_group_sum", "avg_pool", "score_head", "group_queries",
     "mandatory_set", "select_topk", "gather", "compress_layer",
     "two_pass_blockwise", "budgets_inverse_stability", "retained_layout",
     "retained_cache_bytes",
@@ -170,6 +173,16 @@ def gather(k, v, idx):
     return k[idx], v[idx], idx.astype(np.int32)
 
 
+def group_queries(q_b: np.ndarray, h: int, G: int) -> np.ndarray:
+    """Window queries of KV head h as one [G*W, D] block, row g*W + i.
+
+    GQA with contiguous groups: query heads h*G .. h*G + G - 1 share KV head
+    h, i.e. query head g reads KV head g // G.  q_b is [H_q, W, D].
+    """
+    Hq, W, D = q_b.shape
+    return q_b[h * G:(h + 1) * G].reshape(G * W, D)
+
+
 def compress_layer(q_win, k, v, K_l, sink: int, recent: int, pool_k: int,
                    heads=None) -> dict:
     """The whole layer-end compress for one layer.
@@ -188,7 +201,7 @@ def compress_layer(q_win, k, v, K_l, sink: int, recent: int, pool_k: int,
     out = {}
     for (b, h) in (heads if heads is not None else
                    [(b, h) for b in range(B) for h in range(Hkv)]):
-        q_grp = qf[b, h * G:(h + 1) * G].reshape(G * W, D)
+        q_grp = group_queries(qf[b], h, G)
         sc = score_head(q_grp, k[b, h], W, pool_k)
         idx = select_topk(sc["s"], int(K_l[h]), sink, recent)
         kh, vh, pos = gather(k[b, h], v[b, h], idx)
@@ -278,18 +291,19 @@ def budgets_inverse_stability(s_stable, total: int, lo: int, hi: int) -> np.ndar
     """Per-KV-head budgets l_i proportional to w_i = 1 / s_i (HeteroCache, Phase 2).
 
     The pages do not print the L_base formula; the reading taken: every head
-    is compressed (no full heads), the exact shares total * w_i / sum(w) are
+    is compressed (no full heads), the shares total * w_i / sum(w) are
     rounded by largest remainder (ties to the lower head index) so that they
-    sum to ``total``, then clamped to [lo, hi] without redistribution.
+    sum to ``total``, then clamped to [lo, hi] without redistribution.  The
+    shares and their remainders are exact rationals (each fp64 score is
+    converted exactly), so the rounding decision involves no floating-point
+    error at all.
     """
-    s = [float(x) for x in np.asarray(s_stable, dtype=np.float64)]
+    s = [Fraction(float(x)) for x in np.asarray(s_stable, dtype=np.float64)]
     if any(x <= 0 for x in s):
         raise ValueError("stability scores must be > 0")
-    w = [1.0 / x for x in s]
-    wsum = 0.0
-    for x in w:                      # plain left-to-right sum, in head order
-        wsum += x
-    exact = [total * x / wsum for x in w]
+    w = [1 / x for x in s]
+    wsum = sum(w, Fraction(0))
+    exact = [Fraction(int(total)) * x / wsum for x in w]
     base = [math.floor(x) for x in exact]
     short = int(total - sum(base))
     rem = [x - b for x, b in zip(exact, base)]

@@ -28,6 +28,9 @@ def _suite():
         lambda: pins.test_select_invariants_random(),
         lambda: pins.test_softmax_special_case_and_raw_dot_ranking(),
         lambda: pins.test_inverse_stability_budgets(),
+        lambda: pins.test_gather_golden_position_rows(GOLDEN),
+        lambda: pins.test_compress_layer_rows_are_the_selected_positions(),
+        lambda: pins.test_gqa_head_map_hand_case(),
     ]
     failed = 0
     for c in checks:
@@ -129,7 +132,32 @@ def _budget_proportional_to_s(s_stable, total, lo, hi):
     return np.clip(base, lo, hi).astype(np.int32)
 
 
+def _gather_off_by_one(k, v, idx):
+    idx = np.minimum(np.asarray(idx, dtype=np.int64) + 1, len(k) - 1)
+    return k[idx], v[idx], idx.astype(np.int32)
+
+
+def _gather_reversed(k, v, idx):
+    idx = np.asarray(idx, dtype=np.int64)[::-1].copy()
+    return k[idx], v[idx], idx.astype(np.int32)
+
+
+def _gather_swaps_kv(k, v, idx):
+    idx = np.asarray(idx, dtype=np.int64)
+    return v[idx], k[idx], idx.astype(np.int32)
+
+
+def _head_map_modulo(q_b, h, G):
+    Hq, W, D = q_b.shape
+    Hkv = Hq // G
+    return q_b[[g for g in range(Hq) if g % Hkv == h]].reshape(G * W, D)
+
+
 MUTANTS = {
+    "gather_off_by_one": ("gather", _gather_off_by_one),
+    "gather_reversed": ("gather", _gather_reversed),
+    "gather_swaps_kv": ("gather", _gather_swaps_kv),
+    "head_map_modulo": ("group_queries", _head_map_modulo),
     "scale_1_over_D": ("dense_logits", _logits_scale_1_over_D),
     "mask_off_by_one": ("dense_logits", _logits_mask_off_by_one),
     "rows_grouped_wrong": ("dense_logits", _logits_rows_grouped_wrong),

@@ -199,14 +199,67 @@ def test_select_mandatory_union_and_errors():
     assert O.select_topk(np.ones(10), 12, 2, 3).tolist() == list(range(10))
 
 
-def test_gather_rows_and_positions():
-    rng = np.random.default_rng(1)
-    k = rng.standard_normal((30, 4)).astype(np.float32)
-    v = rng.standard_normal((30, 4)).astype(np.float32)
-    idx = np.array([0, 3, 7, 29])
-    kh, vh, pos = O.gather(k, v, idx)
-    assert np.array_equal(kh, k[idx]) and np.array_equal(vh, v[idx])
-    assert pos.dtype == np.int32 and pos.tolist() == idx.tolist()
+def test_gather_golden_position_rows(golden_dir):
+    """K/V rows that encode their own position come back in selection order."""
+    import torch
+    g = json.load(open(os.path.join(golden_dir, "gather_positions.json")))
+    S, D = g["S"], g["D"]
+    j = torch.arange(S, dtype=torch.float32)
+    k = torch.stack([j, -j], dim=1).to(torch.bfloat16)
+    v = torch.stack([100 + j, -100 - j], dim=1).to(torch.bfloat16)
+    assert k.shape == (S, D)
+    kh, vh, pos = O.gather(k, v, np.array(g["idx"]))
+    assert kh.dtype == torch.bfloat16 and vh.dtype == torch.bfloat16
+    assert kh.float().tolist() == g["k_hat"]
+    assert vh.float().tolist() == g["v_hat"]
+    assert pos.dtype == np.int32 and pos.tolist() == g["pos"]
+
+
+def test_compress_layer_rows_are_the_selected_positions():
+    """The retained rows of a whole compress are the rows at its own (ascending) positions."""
+    import torch
+    rng = np.random.default_rng(3)
+    B, Hq, Hkv, S, D, W = 1, 4, 2, 48, 4, 4
+    q = torch.from_numpy(rng.standard_normal((B, Hq, W, D))).to(torch.bfloat16)
+    j = torch.arange(S, dtype=torch.float32)[:, None]
+    noise = torch.from_numpy(rng.standard_normal((B, Hkv, S, D - 1))).float()
+    k = torch.cat([j.expand(B, Hkv, S, 1), noise], dim=3).to(torch.bfloat16)   # column 0 = position
+    v = (-1 - j).expand(B, Hkv, S, D).to(torch.bfloat16)                      # exact: |v| <= 256
+    out = O.compress_layer(q, k, v, [10, 17], 2, 4, 3)
+    for (b, h), r in out.items():
+        pos = r["pos"].tolist()
+        assert pos == sorted(set(pos)) and len(pos) == [10, 17][h]
+        assert r["k_hat"][:, 0].float().tolist() == pos
+        assert r["v_hat"][:, 0].float().tolist() == [-1 - p for p in pos]
+
+
+def test_gqa_head_map_hand_case():
+    """Hand-built GQA case: the scores follow from the head map g -> g // G.
+
+    H_q=4, H_kv=2 (G=2), W=1, D=2, S=8.  KV head 0 has one non-zero key, at
+    position 3, equal to (c, 0); KV head 1 has one, at position 5, equal to
+    (0, c); c = 4*sqrt(2), so q.k/sqrt(D) = 4 for an aligned query.  Query
+    heads 0 and 1 are (1, 0), heads 2 and 3 are (0, 1).  With contiguous
+    groups each KV head sees two aligned queries, so for the single window
+    query (t = 7, all keys visible) the heavy key gets 2 e^4 / (e^4 + 7) and
+    every other key 2 / (e^4 + 7).  Any other map puts an orthogonal query
+    (uniform weights 1/8) in the group.
+    """
+    S, D, W = 8, 2, 1
+    c = 4 * math.sqrt(2)
+    k = np.zeros((1, 2, S, D))
+    k[0, 0, 3] = (c, 0.0)
+    k[0, 1, 5] = (0.0, c)
+    q = np.zeros((1, 4, W, D))
+    q[0, 0:2, 0] = (1.0, 0.0)
+    q[0, 2:4, 0] = (0.0, 1.0)
+    out = O.compress_layer(q, k, np.zeros_like(k), [3, 3], 1, 1, 1)
+    den = math.exp(4) + 7
+    for h, heavy in ((0, 3), (1, 5)):
+        want = np.full(S, 2 / den)
+        want[heavy] = 2 * math.exp(4) / den
+        np.testing.assert_allclose(out[(0, h)]["r"], want, rtol=1e-13)
+        assert out[(0, h)]["idx"].tolist() == sorted({0, heavy, 7})
 
 
 # --------------------------------------------------- closed forms from pages
@@ -231,6 +284,10 @@ def test_inverse_stability_budgets():
     assert K2.tolist() == [50, 50, 200]
     # largest remainder, ties to the lower head index
     assert O.budgets_inverse_stability(np.ones(3), 10, 0, 100).tolist() == [4, 3, 3]
+    # worked by hand: s = (1, 2, 4) -> w = (1, 1/2, 1/4), shares 10 w / (7/4) =
+    # (40/7, 20/7, 10/7); floors (5, 2, 1) leave 2; remainders (5/7, 6/7, 3/7)
+    # give them to heads 1 and 0
+    assert O.budgets_inverse_stability(np.array([1.0, 2.0, 4.0]), 10, 0, 100).tolist() == [6, 3, 1]
 
 
 def test_retained_layout():
