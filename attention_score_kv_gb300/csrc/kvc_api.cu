@@ -155,9 +155,9 @@ bool layout_ws(int B, int H_q, int H_kv, int D, int W, int b_s, int K_l_max, int
 
 using namespace kvc;
 
-namespace {
+namespace kvc {
 
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_shapes(int B, int H_q, int H_kv, int S, int D, int W) {
   if (B < 1 || H_q < 1 || H_kv < 1 || S < 1 || W < 1)
@@ -200,8 +200,46 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
   return KVC_OK;
 }
 
-// Selection parameters from the host budget array.
-int make_sel(int S, int H_kv, const int32_t* K_l, int sink, int recent, SelParams* sp, int* K_l_eff_max) {
+}  // namespace kvc
+
+namespace {
+
+// Rows of each head inside a batch element's block of the retained cache:
+// head h fills min(K_l[h], S) rows from out_off[h]; the block is
+// out_off[H_kv] rows long.  out_off NULL: the packed layout of
+// kvc_retained_layout.  K_l[h] >= lo_rows is required.
+int make_layout(int S, int H_kv, const int32_t* K_l, const int64_t* out_off, int lo_rows, SelParams* sp) {
+  if (!K_l) return set_error(KVC_ERR_INVALID_ARG, "K_l is NULL");
+  int64_t off = 0;
+  for (int h = 0; h < H_kv; ++h) {
+    if (K_l[h] < 0) return set_error(KVC_ERR_INVALID_ARG, "K_l[%d]=%d is negative", h, K_l[h]);
+    if (K_l[h] < lo_rows)
+      return set_error(KVC_ERR_INVALID_ARG, "K_l[%d]=%d is smaller than the mandatory set (%d keys)", h, K_l[h],
+                       lo_rows);
+    const int kept = std::min(K_l[h], S);
+    if (out_off) {
+      if (out_off[h] < off)
+        return set_error(KVC_ERR_INVALID_ARG, "out_off[%d]=%lld overlaps the rows before it (need >= %lld)", h,
+                         (long long)out_off[h], (long long)off);
+      off = out_off[h];
+    }
+    sp->kept[h] = kept;
+    sp->off[h] = off;
+    off += kept;
+  }
+  if (out_off) {
+    if (out_off[H_kv] < off)
+      return set_error(KVC_ERR_INVALID_ARG, "out_off[%d]=%lld is shorter than the rows of the last head (need >= %lld)",
+                       H_kv, (long long)out_off[H_kv], (long long)off);
+    off = out_off[H_kv];
+  }
+  sp->T = off;
+  return KVC_OK;
+}
+
+// Selection parameters from the host budget array and the output layout.
+int make_sel(int S, int H_kv, const int32_t* K_l, const int64_t* out_off, int sink, int recent, SelParams* sp,
+             int* K_l_eff_max) {
   if (!K_l) return set_error(KVC_ERR_INVALID_ARG, "K_l is NULL");
   if (sink < 0 || recent < 0) return set_error(KVC_ERR_INVALID_ARG, "sink/recent must be >= 0");
   std::memset(sp, 0, sizeof(*sp));
@@ -213,18 +251,13 @@ int make_sel(int S, int H_kv, const int32_t* K_l, int sink, int recent, SelParam
   sp->r_lo = std::min(sink, S);
   sp->r_hi = std::max(S - std::min(recent, S), sp->r_lo);
   const int rsz = sp->r_lo + (S - sp->r_hi);
-  int64_t off = 0;
+  int rc = make_layout(S, H_kv, K_l, out_off, rsz, sp);
+  if (rc) return rc;
   int mx = 0;
   for (int h = 0; h < H_kv; ++h) {
-    if (K_l[h] < rsz)
-      return set_error(KVC_ERR_INVALID_ARG, "K_l[%d]=%d is smaller than the mandatory set (%d keys)", h, K_l[h], rsz);
-    const int kept = std::min(K_l[h], S);
-    sp->n_sel[h] = kept - rsz;
-    sp->off[h] = off;
-    off += kept;
-    mx = std::max(mx, kept);
+    sp->n_sel[h] = sp->kept[h] - rsz;
+    mx = std::max(mx, sp->kept[h]);
   }
-  sp->T = off;
   if (K_l_eff_max) *K_l_eff_max = mx;
   return KVC_OK;
 }
@@ -242,8 +275,8 @@ namespace {
 // are read by the gather only).
 int compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int D, int W, const int32_t* K_l,
                    int sink, int recent, int pool_k, int b_s, const kvc_bf16* q_win, const kvc_bf16* k,
-                   const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, void* ws,
-                   size_t ws_bytes, cudaEvent_t v_ready, kvc_stream_t stream) {
+                   const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out,
+                   const int64_t* out_off, void* ws, size_t ws_bytes, cudaEvent_t v_ready, kvc_stream_t stream) {
   int rc;
   if (N < 1 || layer < 0 || layer >= N) return set_error(KVC_ERR_INVALID_ARG, "layer %d outside [0, N=%d)", layer, N);
   if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s)) || (rc = check_pool(pool_k))) return rc;
@@ -254,7 +287,7 @@ int compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int
     return rc;
   SelParams sp;
   int kmax = 0;
-  if ((rc = make_sel(S, H_kv, K_l, sink, recent, &sp, &kmax))) return rc;
+  if ((rc = make_sel(S, H_kv, K_l, out_off, sink, recent, &sp, &kmax))) return rc;
   WsLayout L;
   if (!layout_ws(B, H_q, H_kv, D, W, b_s, kmax, pool_k, S, &L)) return set_error(KVC_ERR_CUDA, "no CUDA device");
   if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
@@ -287,14 +320,10 @@ int compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int
                           "selection launch")))
     return rc;
   if (ev) cudaEventRecord(ev[3], st);
-  std::vector<int64_t> off(H_kv + 1);
-  for (int h = 0; h < H_kv; ++h) off[h] = sp.off[h];
-  off[H_kv] = sp.T;
   if (v_ready && (rc = launch_status(cudaStreamWaitEvent(st, v_ready, 0), "wait for v_ready")))
     return rc;
-  rc = launch_status(launch_gather(kk, vv, pos_out, B, H_kv, S, D, sp.T, off.data(),
-                                   reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out),
-                                   pos_out, st),
+  rc = launch_status(launch_gather(kk, vv, pos_out, B, sp, D, reinterpret_cast<__nv_bfloat16*>(k_out),
+                                   reinterpret_cast<__nv_bfloat16*>(v_out), pos_out, st),
                      "gather launch");
   if (ev) cudaEventRecord(ev[4], st);
   return rc;
@@ -306,7 +335,7 @@ extern "C" {
 
 const char* kvc_last_error(void) { return t_err; }
 
-int kvc_version(void) { return 200; }
+int kvc_version(void) { return 300; }
 
 int kvc_set_option(int option, int64_t value) {
   if (option == KVC_OPT_SCAN_CTAS) {
@@ -395,14 +424,14 @@ int kvc_score_rawdot_int8(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H
                        "INT8 raw-product scorer launch");
 }
 
-int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* K_l, int sink, int recent,
-                    int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* K_l, const int64_t* out_off,
+                    int sink, int recent, int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream) {
   int rc;
   if (B < 1 || H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "B, H_kv and S must be >= 1");
   if (H_kv > kMaxHkv) return set_error(KVC_ERR_UNSUPPORTED, "H_kv=%d above %d", H_kv, kMaxHkv);
   if ((rc = check_ptr(scores, 4, "scores")) || (rc = check_ptr(idx, 4, "idx"))) return rc;
   SelParams sp;
-  if ((rc = make_sel(S, H_kv, K_l, sink, recent, &sp, nullptr))) return rc;
+  if ((rc = make_sel(S, H_kv, K_l, out_off, sink, recent, &sp, nullptr))) return rc;
   (void)ws;
   (void)ws_bytes;
   sp.nparts = 1;
@@ -410,8 +439,9 @@ int kvc_select_topk(const float* scores, int B, int H_kv, int S, const int32_t* 
                        "selection launch");
 }
 
-int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx, int B, int H_kv, int S, int D,
-               const int32_t* K_l, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, kvc_stream_t stream) {
+int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx, const int64_t* out_off, int B, int H_kv,
+               int S, int D, const int32_t* K_l, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out,
+               kvc_stream_t stream) {
   int rc;
   if (B < 1 || H_kv < 1 || S < 1) return set_error(KVC_ERR_INVALID_ARG, "B, H_kv and S must be >= 1");
   if (D != 64 && D != 128) return set_error(KVC_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are supported", D);
@@ -420,34 +450,32 @@ int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx, int B, 
       (rc = check_ptr(k_out, 16, "k_out")) || (rc = check_ptr(v_out, 16, "v_out")) ||
       (rc = check_ptr(pos_out, 4, "pos_out")))
     return rc;
-  if (!K_l) return set_error(KVC_ERR_INVALID_ARG, "K_l is NULL");
-  std::vector<int64_t> off(H_kv + 1, 0);
-  for (int h = 0; h < H_kv; ++h) {
-    if (K_l[h] < 0) return set_error(KVC_ERR_INVALID_ARG, "K_l[%d]=%d is negative", h, K_l[h]);
-    off[h + 1] = off[h] + std::min(K_l[h], S);
-  }
+  SelParams sp{};
+  sp.S = S;
+  sp.H_kv = H_kv;
+  if ((rc = make_layout(S, H_kv, K_l, out_off, 0, &sp))) return rc;
   return launch_status(
-      launch_gather(reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), idx, B, H_kv,
-                    S, D, off[H_kv], off.data(), reinterpret_cast<__nv_bfloat16*>(k_out),
-                    reinterpret_cast<__nv_bfloat16*>(v_out), pos_out, reinterpret_cast<cudaStream_t>(stream)),
+      launch_gather(reinterpret_cast<const __nv_bfloat16*>(k), reinterpret_cast<const __nv_bfloat16*>(v), idx, B, sp,
+                    D, reinterpret_cast<__nv_bfloat16*>(k_out), reinterpret_cast<__nv_bfloat16*>(v_out), pos_out,
+                    reinterpret_cast<cudaStream_t>(stream)),
       "gather launch");
 }
 
 int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q, int H_kv, int D, int W, const int32_t* K_l,
                        int sink, int recent, int pool_k, int b_s, const kvc_bf16* q_win, const kvc_bf16* k,
-                       const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out, void* ws,
-                       size_t ws_bytes, kvc_stream_t stream) {
+                       const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out,
+                       const int64_t* out_off, void* ws, size_t ws_bytes, kvc_stream_t stream) {
   return compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, pool_k, b_s, q_win, k, v, k_out,
-                        v_out, pos_out, ws, ws_bytes, nullptr, stream);
+                        v_out, pos_out, out_off, ws, ws_bytes, nullptr, stream);
 }
 
 int kvc_compress_layer_deferred_v(int N, int layer, int B, int S, int C, int H_q, int H_kv, int D, int W,
                                   const int32_t* K_l, int sink, int recent, int pool_k, int b_s,
                                   const kvc_bf16* q_win, const kvc_bf16* k, const kvc_bf16* v, kvc_bf16* k_out,
-                                  kvc_bf16* v_out, int32_t* pos_out, void* ws, size_t ws_bytes,
-                                  kvc_event_t v_ready, kvc_stream_t stream) {
+                                  kvc_bf16* v_out, int32_t* pos_out, const int64_t* out_off, void* ws,
+                                  size_t ws_bytes, kvc_event_t v_ready, kvc_stream_t stream) {
   return compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, pool_k, b_s, q_win, k, v, k_out,
-                        v_out, pos_out, ws, ws_bytes, reinterpret_cast<cudaEvent_t>(v_ready), stream);
+                        v_out, pos_out, out_off, ws, ws_bytes, reinterpret_cast<cudaEvent_t>(v_ready), stream);
 }
 
 int kvc_scan_ranges(int BH, int S, int P, int64_t* starts) {

@@ -87,11 +87,19 @@ struct SelParams {
   int64_t L;            // scan plan (candidate-list mode)
   int maxseg;
   int n_sel[kMaxHkv];   // non-mandatory keys kept per head (or all candidates)
+  int kept[kMaxHkv];    // rows head h fills: min(K_l[h], S)
   int64_t off[kMaxHkv]; // row offset of head h inside a batch element
 };
 
 // ------------------------------------------------------------ host helpers
 int set_error(int code, const char* fmt, ...);
+// Argument checks shared by the entry points (KVC_OK or an error code with
+// the message set).
+int check_shapes(int B, int H_q, int H_kv, int S, int D, int W);
+int check_bs(int b_s);
+int check_pool(int pool_k);
+int check_ptr(const void* p, size_t align, const char* name);
+int check_ws(void* ws, size_t ws_bytes, size_t need);
 int cuda_error(cudaError_t e, const char* what);
 int num_sms();
 int scan_ctas_target();                             // SM count or the tuning override
@@ -161,9 +169,11 @@ cudaError_t launch_budget(const double* s_stable, int n_layers, int H, int64_t t
 // selection over dense scores (mode 0) or candidate lists (mode 1)
 cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, const int* cand_cnt, int cap, int B,
                           const SelParams& sel, int32_t* idx, cudaStream_t st);
-cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* idx, int B, int H_kv,
-                          int S, int D, int64_t T, const int64_t* off_host, __nv_bfloat16* k_out,
-                          __nv_bfloat16* v_out, int32_t* pos_out, cudaStream_t st);
+// rows of head h inside a batch element: off[h] .. off[h] + kept[h] - 1 of a
+// T-row block; other rows of the block are left untouched
+cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* idx, int B,
+                          const SelParams& sel, int D, __nv_bfloat16* k_out, __nv_bfloat16* v_out,
+                          int32_t* pos_out, cudaStream_t st);
 
 int* status_word_ptr();     // device address of the status word
 void note_launches(int n);  // count kernels issued (measurement)

@@ -49,8 +49,6 @@ int scratch_on_current_device(float** out) {
   return KVC_OK;
 }
 
-bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 }  // namespace kvc
 
@@ -59,23 +57,15 @@ using namespace kvc;
 extern "C" int kvc_score_pass1_noalloc(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q, int H_kv,
                                        int S, int D, int W, int b_s, float* m, float* Z,
                                        kvc_stream_t stream) {
-  if (B < 1 || H_q < 1 || H_kv < 1 || S < 1 || W < 1)
-    return set_error(KVC_ERR_INVALID_ARG, "B, H_q, H_kv, S and W must be >= 1");
-  if (H_q % H_kv != 0) return set_error(KVC_ERR_INVALID_ARG, "H_q (%d) must be a multiple of H_kv (%d)", H_q, H_kv);
-  if (W > S) return set_error(KVC_ERR_INVALID_ARG, "W (%d) must be <= S (%d)", W, S);
-  if (S > (1 << 30)) return set_error(KVC_ERR_UNSUPPORTED, "S (%d) above 2^30", S);
-  if (D != 64 && D != 128) return set_error(KVC_ERR_UNSUPPORTED, "head dim D=%d: only 64 and 128 are supported", D);
-  if ((H_q / H_kv) * W > kMaxGWP)
-    return set_error(KVC_ERR_UNSUPPORTED, "G*W=%d above %d window rows per KV head", (H_q / H_kv) * W, kMaxGWP);
-  if (b_s < kTile) return set_error(KVC_ERR_INVALID_ARG, "b_s=%d must be >= %d", b_s, kTile);
-  if (!q_win || !k || !m || !Z) return set_error(KVC_ERR_INVALID_ARG, "q_win, k, m and Z must be non-NULL");
-  if (!is_aligned(q_win, 16) || !is_aligned(k, 16)) return set_error(KVC_ERR_INVALID_ARG, "q_win and k must be 16-byte aligned");
-  if (!is_aligned(m, 4) || !is_aligned(Z, 4)) return set_error(KVC_ERR_INVALID_ARG, "m and Z must be 4-byte aligned");
+  int rc;
+  if ((rc = check_shapes(B, H_q, H_kv, S, D, W)) || (rc = check_bs(b_s))) return rc;
+  if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(m, 4, "m")) ||
+      (rc = check_ptr(Z, 4, "Z")))
+    return rc;
 
   // Partials need 2 * gwp floats per (scan CTA, KV head it touches).  Use the
   // default scan plan when its partials fit the fixed array, else one CTA per
   // head (one slot per head); refuse shapes where even that does not fit.
-  if ((int64_t)B * H_kv > (1LL << 24)) return set_error(KVC_ERR_UNSUPPORTED, "batch too large");
   const int BH = B * H_kv;
   const int gwp = ((H_q / H_kv) * W + 15) / 16 * 16;
   const int64_t per_slot = (int64_t)gwp * 2;
@@ -90,7 +80,7 @@ extern "C" int kvc_score_pass1_noalloc(const kvc_bf16* q_win, const kvc_bf16* k,
   const int64_t slots = (int64_t)pl.P * pl.maxseg;
 
   float* scratch = nullptr;
-  int rc = scratch_on_current_device(&scratch);
+  rc = scratch_on_current_device(&scratch);
   if (rc != KVC_OK) return rc;
   float* pm = scratch;
   float* pz = scratch + slots * gwp;

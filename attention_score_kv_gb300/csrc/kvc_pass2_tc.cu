@@ -321,45 +321,42 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[buf]));
-        const int j = t0 + krow;
-        const bool need_mask = (t0 + kTile - 1 > A.S - A.W);
-        float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-        if (!need_mask) {
-          if (c0 + 4 > c_end) {
+        // Columns that carry no weight become -inf (2^-inf = 0): chunks
+        // past this warp's slice, and, in tiles near the window, the window
+        // queries a key comes after (query i of column g*W + i sees key j
+        // only when j <= S - W + i).  Every key then runs the same
+        // arithmetic in the same order, so keys with equal inputs get
+        // bit-identical masses wherever they sit.
+        if (c0 + 4 > c_end) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              if (c0 + i >= c_end) {
+          for (int i = 0; i < 4; ++i)
+            if (c0 + i >= c_end) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) v[16 * i + q] = -INFINITY;
-              }
-          }
+              for (int q = 0; q < 16; ++q) v[16 * i + q] = -INFINITY;
+            }
+        }
+        if (t0 + kTile - 1 > A.S - A.W) {
+          const int dj = t0 + krow - (A.S - A.W);
+          if (dj > 0) {
+            int wi = (c0 * 16) % A.W;
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            const float2 x0 = __fmul2_rn(make_float2(v[c], v[c + 1]), cc);
-            const float2 x1 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), cc);
-            const float2 x2 = __fmul2_rn(make_float2(v[c + 4], v[c + 5]), cc);
-            const float2 x3 = __fmul2_rn(make_float2(v[c + 6], v[c + 7]), cc);
-            a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
-            a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
-            a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
-            a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
-          }
-        } else {
-          // tiles near the window: window query i (column g*W + i) sees key
-          // j only when j <= S - W + i, i.e. i >= dj
-          const int dj = j - (A.S - A.W);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (c0 + i < c_end) {
-              int wi = ((c0 + i) * 16) % A.W;
-#pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                const float e = ex2(v[16 * i + q] * c2);
-                a0.x += wi >= dj ? e : 0.f;
-                if (++wi == A.W) wi = 0;
-              }
+            for (int c = 0; c < 64; ++c) {
+              if (wi < dj) v[c] = -INFINITY;
+              if (++wi == A.W) wi = 0;
             }
           }
+        }
+        float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+          const float2 x0 = __fmul2_rn(make_float2(v[c], v[c + 1]), cc);
+          const float2 x1 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), cc);
+          const float2 x2 = __fmul2_rn(make_float2(v[c + 4], v[c + 5]), cc);
+          const float2 x3 = __fmul2_rn(make_float2(v[c + 6], v[c + 7]), cc);
+          a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
+          a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
+          a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
+          a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
         }
         const float r = (a0.x + a0.y) + (a1.x + a1.y) + ((a2.x + a2.y) + (a3.x + a3.y));
         const int slot = tcount % kRing;

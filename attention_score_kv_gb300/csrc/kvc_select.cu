@@ -497,6 +497,7 @@ kvc_gather_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
       const int mid = (lo + hi + 1) >> 1;
       if (sp.off[mid] <= within) lo = mid; else hi = mid - 1;
     }
+    if (within < sp.off[lo] || within - sp.off[lo] >= sp.kept[lo]) continue;   // a row the layout leaves free
     const int j = idx[r];
     if (j < 0 || j >= sp.S) {
       if (cl == 0) record_status(status, kStatusSelectMismatch);
@@ -592,13 +593,9 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* idx, int B,
-                          int H_kv, int S, int D, int64_t T, const int64_t* off_host,
-                          __nv_bfloat16* k_out, __nv_bfloat16* v_out, int32_t* pos_out, cudaStream_t st) {
-  SelParams sp{};
-  sp.S = S;
-  sp.H_kv = H_kv;
-  sp.T = T;
-  for (int h = 0; h < H_kv; ++h) sp.off[h] = off_host[h];
+                          const SelParams& sp, int D, __nv_bfloat16* k_out, __nv_bfloat16* v_out,
+                          int32_t* pos_out, cudaStream_t st) {
+  const int64_t T = sp.T;
   const int64_t rows = (int64_t)B * T;
   if (rows == 0) return cudaSuccess;
   const int rows_per_block = (256 / 32) * (32 / (D / 8));

@@ -63,12 +63,12 @@ _SIGS = {
     "kvc_score_pass1_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_score_pass2_pool": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "kvc_score_rawdot_int8": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
-    "kvc_select_topk": (_I, [_P, _I, _I, _I, _I32P, _I, _I, _P, _P, _SZ, _P]),
-    "kvc_gather": (_I, [_P, _P, _P, _I, _I, _I, _I, _I32P, _P, _P, _P, _P]),
+    "kvc_select_topk": (_I, [_P, _I, _I, _I, _I32P, _I64P, _I, _I, _P, _P, _SZ, _P]),
+    "kvc_gather": (_I, [_P, _P, _P, _I64P, _I, _I, _I, _I, _I32P, _P, _P, _P, _P]),
     "kvc_compress_layer": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I32P, _I, _I, _I, _I,
-                                _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+                                _P, _P, _P, _P, _P, _P, _I64P, _P, _SZ, _P]),
     "kvc_compress_layer_deferred_v": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I32P, _I, _I, _I, _I,
-                                           _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+                                           _P, _P, _P, _P, _P, _P, _I64P, _P, _SZ, _P, _P]),
     "kvc_overlap_coefficient": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "kvc_head_similarity": (_I, [_P, _P, _I, _I, _P, _P]),
     "kvc_budget_inverse_stability_device": (_I, [_I, _I, _P, _I64, _I, _I, _P, _P]),
@@ -117,6 +117,14 @@ def _stream(stream) -> int | None:
 def _i32(arr):
     vals = [int(x) for x in (arr.tolist() if hasattr(arr, "tolist") else arr)]
     return (ctypes.c_int32 * len(vals))(*vals)
+
+
+def _i64_or_null(arr):
+    """A host int64 array, or NULL for None (the packed output layout)."""
+    if arr is None:
+        return None
+    vals = [int(x) for x in (arr.tolist() if hasattr(arr, "tolist") else arr)]
+    return (ctypes.c_int64 * len(vals))(*vals)
 
 
 def kvc_last_error() -> str:
@@ -191,21 +199,22 @@ def kvc_budget_inverse_stability_device(n_layers, H_kv, s_stable, total, lo, hi,
                                                     _stream(stream)))
 
 
-def kvc_select_topk(scores, B, H_kv, S, K_l, sink, recent, idx, ws, ws_bytes=None, stream=None):
-    _check(_lib.kvc_select_topk(_ptr(scores), B, H_kv, S, _i32(K_l), sink, recent, _ptr(idx), _ptr(ws),
-                                ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
+def kvc_select_topk(scores, B, H_kv, S, K_l, sink, recent, idx, ws, ws_bytes=None, stream=None, out_off=None):
+    _check(_lib.kvc_select_topk(_ptr(scores), B, H_kv, S, _i32(K_l), _i64_or_null(out_off), sink, recent, _ptr(idx),
+                                _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
 
 
-def kvc_gather(k, v, idx, B, H_kv, S, D, K_l, k_out, v_out, pos_out, stream=None):
-    _check(_lib.kvc_gather(_ptr(k), _ptr(v), _ptr(idx), B, H_kv, S, D, _i32(K_l), _ptr(k_out), _ptr(v_out),
-                           _ptr(pos_out), _stream(stream)))
+def kvc_gather(k, v, idx, B, H_kv, S, D, K_l, k_out, v_out, pos_out, stream=None, out_off=None):
+    _check(_lib.kvc_gather(_ptr(k), _ptr(v), _ptr(idx), _i64_or_null(out_off), B, H_kv, S, D, _i32(K_l),
+                           _ptr(k_out), _ptr(v_out), _ptr(pos_out), _stream(stream)))
 
 
 def kvc_compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, pool_k, b_s, q_win, k, v,
-                       k_out, v_out, pos_out, ws, ws_bytes=None, stream=None):
+                       k_out, v_out, pos_out, ws, ws_bytes=None, stream=None, out_off=None):
     _check(_lib.kvc_compress_layer(N, layer, B, S, C, H_q, H_kv, D, W, _i32(K_l), sink, recent, pool_k, b_s,
                                    _ptr(q_win), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out), _ptr(pos_out),
-                                   _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes, _stream(stream)))
+                                   _i64_or_null(out_off), _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
+                                   _stream(stream)))
 
 
 def _event(ev) -> int | None:
@@ -215,13 +224,14 @@ def _event(ev) -> int | None:
 
 
 def kvc_compress_layer_deferred_v(N, layer, B, S, C, H_q, H_kv, D, W, K_l, sink, recent, pool_k, b_s, q_win, k, v,
-                                  k_out, v_out, pos_out, ws, v_ready, ws_bytes=None, stream=None):
+                                  k_out, v_out, pos_out, ws, v_ready, ws_bytes=None, stream=None, out_off=None):
     """kvc_compress_layer whose gather first waits on the event v_ready
     (e.g. recorded after v's host-to-device copy on another stream)."""
     _check(_lib.kvc_compress_layer_deferred_v(N, layer, B, S, C, H_q, H_kv, D, W, _i32(K_l), sink, recent, pool_k,
                                               b_s, _ptr(q_win), _ptr(k), _ptr(v), _ptr(k_out), _ptr(v_out),
-                                              _ptr(pos_out), _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
-                                              _event(v_ready), _stream(stream)))
+                                              _ptr(pos_out), _i64_or_null(out_off), _ptr(ws),
+                                              ws.numel() if ws_bytes is None else ws_bytes, _event(v_ready),
+                                              _stream(stream)))
 
 
 def kvc_scan_ranges(BH, S, P) -> list:

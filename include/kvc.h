@@ -149,31 +149,52 @@ int kvc_score_rawdot_int8(const kvc_bf16* q_win, const kvc_bf16* k, int B,
                           kvc_stream_t stream);
 
 /*
+ * Output layout shared by kvc_select_topk, kvc_gather and kvc_compress_layer
+ * (TideKV Fig. 2: the layer's retained cache, one block of rows per batch
+ * element).  out_off is a HOST int64 array [H_kv + 1], or NULL:
+ *  - NULL: the packed layout of kvc_retained_layout -- head h owns rows
+ *    off[h] .. off[h] + min(K_l[h], S) - 1, heads back to back, and a batch
+ *    element's block is T = sum_h min(K_l[h], S) rows long.
+ *  - given: head h fills min(K_l[h], S) rows starting at row out_off[h] of
+ *    its batch element's block, and the block is out_off[H_kv] rows long
+ *    (batch element b starts at row b * out_off[H_kv]).  A caller can so
+ *    keep fixed-size per-head slots (e.g. out_off[h] = h * K_max) or
+ *    leading room; rows a head does not fill are left untouched.  Required:
+ *    out_off[0] >= 0, out_off[h] + min(K_l[h], S) <= out_off[h+1];
+ *    otherwise KVC_ERR_INVALID_ARG before any launch.
+ */
+
+/*
  * Per-head selection (TideKV Fig. 3): keep R_mand and the top
  * (K_l[h] - |R_mand|) other keys by (score descending, index ascending).
- *   scores [B, H_kv, S] fp32, finite, any sign (-0 ranks as +0)
- *   K_l    HOST [H_kv]; K_l[h] >= |R_mand|.  A head with K_l[h] >= S keeps
- *          every key.
- *   idx    out, int32 positions, ascending within each head.  Head h of
- *          batch element b occupies rows b * T + off[h] .. + min(K_l[h], S)
- *          - 1, where off / T come from kvc_retained_layout.
+ *   scores  [B, H_kv, S] fp32, finite, any sign (-0 ranks as +0)
+ *   K_l     HOST [H_kv]; K_l[h] >= |R_mand|.  A head with K_l[h] >= S keeps
+ *           every key.
+ *   out_off HOST [H_kv + 1] or NULL: the output layout (above)
+ *   idx     out, int32 positions, ascending within each head, in the
+ *           layout out_off describes.
  */
 int kvc_select_topk(const float* scores, int B, int H_kv, int S,
-                    const int32_t* K_l, int sink, int recent, int32_t* idx,
-                    void* ws, size_t ws_bytes, kvc_stream_t stream);
+                    const int32_t* K_l, const int64_t* out_off, int sink,
+                    int recent, int32_t* idx, void* ws, size_t ws_bytes,
+                    kvc_stream_t stream);
 
 /*
  * Gather of the retained cache (TideKV Fig. 2): copy K and V rows at the
  * selected positions and record the positions.
- *   k, v   [B, H_kv, S, D] bf16
- *   idx    int32 positions in the layout of kvc_select_topk (values in [0,S))
- *   k_out, v_out [B * T, D] bf16 out, pos_out [B * T] int32 out
+ *   k, v    [B, H_kv, S, D] bf16
+ *   idx     int32 positions in the layout out_off and K_l describe (the
+ *           first min(K_l[h], S) rows of each head's slot, values in [0,S))
+ *   out_off HOST [H_kv + 1] or NULL: the output layout (above)
+ *   k_out, v_out [B * T, D] bf16 out, pos_out [B * T] int32 out (T the
+ *           block length of the layout); only the rows the heads fill are
+ *           written
  * idx and pos_out may be the same buffer.
  */
 int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx,
-               int B, int H_kv, int S, int D, const int32_t* K_l,
-               kvc_bf16* k_out, kvc_bf16* v_out, int32_t* pos_out,
-               kvc_stream_t stream);
+               const int64_t* out_off, int B, int H_kv, int S, int D,
+               const int32_t* K_l, kvc_bf16* k_out, kvc_bf16* v_out,
+               int32_t* pos_out, kvc_stream_t stream);
 
 /*
  * The whole layer-end compress of layer `layer` (TideKV Fig. 2 and 3):
@@ -181,7 +202,8 @@ int kvc_gather(const kvc_bf16* k, const kvc_bf16* v, const int32_t* idx,
  * per layer after all of its prompt chunks, before the next layer starts.
  * N, layer and C are the pages' symbols and are only validated:
  * 0 <= layer < N and 1 <= W <= C <= S (the window is the tail of the last
- * chunk); C does not change the result.  Outputs as kvc_gather.
+ * chunk); C does not change the result.  Outputs as kvc_gather, in the
+ * layout out_off describes (NULL: packed).
  * The per-head score vector is never materialised: each key range keeps a
  * candidate list of at most K_l_max + b_s keys in `ws`.
  */
@@ -190,8 +212,8 @@ int kvc_compress_layer(int N, int layer, int B, int S, int C, int H_q,
                        int recent, int pool_k, int b_s,
                        const kvc_bf16* q_win, const kvc_bf16* k,
                        const kvc_bf16* v, kvc_bf16* k_out, kvc_bf16* v_out,
-                       int32_t* pos_out, void* ws, size_t ws_bytes,
-                       kvc_stream_t stream);
+                       int32_t* pos_out, const int64_t* out_off, void* ws,
+                       size_t ws_bytes, kvc_stream_t stream);
 
 /*
  * kvc_compress_layer for callers that upload the values while the scans
@@ -211,7 +233,8 @@ int kvc_compress_layer_deferred_v(int N, int layer, int B, int S, int C,
                                   int pool_k, int b_s, const kvc_bf16* q_win,
                                   const kvc_bf16* k, const kvc_bf16* v,
                                   kvc_bf16* k_out, kvc_bf16* v_out,
-                                  int32_t* pos_out, void* ws, size_t ws_bytes,
+                                  int32_t* pos_out, const int64_t* out_off,
+                                  void* ws, size_t ws_bytes,
                                   kvc_event_t v_ready, kvc_stream_t stream);
 
 /*

@@ -53,7 +53,17 @@ def test_workspace_size_has_no_S_argument():
 
 
 def test_version(K):
-    assert K.kvc_version() == 200
+    assert K.kvc_version() == 300
+
+
+def test_boundary_takes_the_output_layout():
+    """kvc_select_topk, kvc_gather and kvc_compress_layer(_deferred_v) take a
+    caller-supplied CSR output layout (const int64_t* out_off), as the
+    boundary's call list has them."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for fn in ("kvc_select_topk", "kvc_gather", "kvc_compress_layer", "kvc_compress_layer_deferred_v"):
+        m = re.search(fn + r"\(([^)]*)\)", src, flags=re.S)
+        assert m and "const int64_t* out_off" in m.group(1), fn
 
 
 def _call_compress(K, **over):
@@ -77,6 +87,9 @@ def _call_compress(K, **over):
     (dict(q_win=0), -1),               # null pointer
     (dict(k=0x2004), -1),              # misaligned bf16 tensor
     (dict(H_q=64, H_kv=2, W=16), -2),  # G*W = 512 > 256
+    (dict(out_off=[-1, 128, 256]), -1),        # layout starts before row 0
+    (dict(out_off=[0, 100, 256]), -1),         # head 0 fills 128 rows, its slot holds 100
+    (dict(out_off=[0, 128, 200]), -1),         # the block ends inside head 1's rows
 ])
 def test_compress_layer_rejects_bad_arguments(K, over, code):
     with pytest.raises(K.KvcError) as ei:
@@ -110,6 +123,14 @@ def test_budget_below_mandatory_set_is_rejected_before_launch(K):
     # |R_mand| = 4 + 16 = 20 > 19; checked on the host (no device needed to fail)
     with pytest.raises(K.KvcError) as ei:
         K.kvc_select_topk(0x1000, 1, 2, 512, [19, 128], 4, 16, 0x2000, 0x10000, 1 << 20, stream=0)
+    assert ei.value.code == -1
+    with pytest.raises(K.KvcError) as ei:    # overlapping head slots
+        K.kvc_select_topk(0x1000, 1, 2, 512, [128, 128], 4, 16, 0x2000, 0x10000, 1 << 20, stream=0,
+                          out_off=[0, 64, 300])
+    assert ei.value.code == -1
+    with pytest.raises(K.KvcError) as ei:    # a gather layout that cannot hold head 1's rows
+        K.kvc_gather(0x1000, 0x2000, 0x3000, 1, 2, 512, 64, [128, 128], 0x4000, 0x5000, 0x6000, stream=0,
+                     out_off=[0, 128, 255])
     assert ei.value.code in (-1, -4)
 
 

@@ -28,8 +28,22 @@ def K():
 def test_prefill_three_layers_into_the_cross_layer_cache(K, D, C):
     cfg = get_config("tiny", N=3, S=700, C=C, H_q=8, H_kv=2, D=D, W=16, K_l=200, recent=16, pool_k=7,
                      hh_frac=0.02, seed=41)
+    _prefill_and_check(K, cfg, [[200, 260], [200, 150], [700, 40]])   # unequal heads and layers, one keeps all
+
+
+def test_prefill_with_pyramid_budgets(K):
+    """Per-layer budgets from the PyramidKV-style ramp (TideKV-PyramidKV,
+    Tables 3-4) drive the compress of four layers."""
+    cfg = get_config("tiny", N=4, S=900, C=256, H_q=8, H_kv=2, D=128, W=16, K_l=200, recent=16, pool_k=7,
+                     hh_frac=0.02, seed=43)
+    pyr = K.kvc_budget_pyramid(cfg.N, 200, 40)
+    assert pyr == [int(x) for x in LM.budgets_pyramid(cfg.N, 200, 40)]
+    assert sum(pyr) == cfg.N * 200 and pyr == sorted(pyr, reverse=True) and pyr[-1] == 40
+    _prefill_and_check(K, cfg, [[k] * cfg.H_kv for k in pyr])
+
+
+def _prefill_and_check(K, cfg, K_l):
     dev = "cuda"
-    K_l = [[200, 260], [200, 150], [700, 40]]          # unequal heads and layers, one keeps all
     off_layers = K.kvc_cache_layout(cfg.N, cfg.B, cfg.H_kv, cfg.S, K_l)
     assert off_layers == LM.cache_layout(cfg.N, cfg.B, cfg.S, K_l).tolist()
     rows = off_layers[-1]

@@ -227,32 +227,130 @@ def test_workspace_does_not_grow_with_S(K):
 FULL = ["llama8k", "tidekv_main", "mistral128k", "qwen14b"]
 
 
+def _full_size_heads(cfg, K_l_ref):
+    """Heads compared element by element with the oracle at full size: every
+    head of the 8K Llama layer (each is small); for Qwen the heads with the
+    smallest and the largest budget plus the first and last head; else the
+    first and the last head."""
+    if cfg.name == "llama8k":
+        return [(b, h) for b in range(cfg.B) for h in range(cfg.H_kv)]
+    heads = [(0, 0), (cfg.B - 1, cfg.H_kv - 1)]
+    if cfg.inverse_stability:
+        heads += [(1 % cfg.B, int(np.argmin(K_l_ref))), (2 % cfg.B, int(np.argmax(K_l_ref)))]
+    return list(dict.fromkeys(heads))
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_compress_layer(K, name):
     """Full layer shape, the launch configuration the benchmark times; the
-    oracle checks sampled heads, structure is checked on all heads."""
+    oracle checks the heads of _full_size_heads, structure every head."""
     cfg = get_config(name)
     layer = 0
     inp = make_layer_inputs(cfg, layer)
     K_l, K_l_ref = U.kl_vector(cfg, K, layer)
     k_out, v_out, pos, off = U.run_compress(K, cfg, inp, K_l, layer=layer)
     U.check_structure_all_heads(pos, off, cfg, K_l_ref)
-    heads = [(0, 0), (cfg.B - 1, cfg.H_kv - 1)]
-    for (b, h) in heads:
+    for (b, h) in _full_size_heads(cfg, K_l_ref):
         o = U.oracle_head(cfg, inp, b, h)
         U.check_head_outputs(k_out, v_out, pos, off, inp, cfg, b, h, K_l_ref[h], o["s"], f"{name} b={b} h={h}")
 
 
-@pytest.mark.parametrize("name", ["llama8k", "mistral128k"])
+@pytest.mark.parametrize("name", FULL)
 def test_full_size_scores_sampled_heads(K, name):
+    """Element-wise m, Z and pooled scores at full size (the decomposed entry
+    points run the same scan kernels as the compress)."""
     cfg = get_config(name)
     inp = make_layer_inputs(cfg)
     K_l, _ = U.kl_vector(cfg, K)
     out = U.run_decomposed(K, cfg, inp, K_l)
     G = cfg.G
-    for (b, h) in [(0, 3), (cfg.B - 1, cfg.H_kv - 1)]:
+    for (b, h) in [(0, 3 % cfg.H_kv), (cfg.B - 1, cfg.H_kv - 1)]:
         o = U.oracle_head(cfg, inp, b, h)
         U.assert_mz_close(out["m"][b, h * G:(h + 1) * G].reshape(-1), out["Z"][b, h * G:(h + 1) * G].reshape(-1),
                           o, f"{name} b={b} h={h}")
         U.assert_scores_close(out["scores"][b, h].numpy(), o["s"], cfg, f"{name} scores b={b} h={h}")
         assert abs(float(out["scores"][b, h].double().sum()) - o["s"].sum()) < 2e-3 * G * cfg.W
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3])
+def test_all_equal_keys_tie_rule_through_compaction(K, ctas):
+    """Every key equal: each window query weighs the keys it sees equally, so
+    every interior key gets the same mass and, on the GPU, bit-identical fp32
+    scores (one thread per key, the same arithmetic on the same values).  The
+    lower index wins ties, so the kept set is exactly the lowest-index
+    interior keys, here through the fused path's candidate compaction
+    (few scan CTAs, key ranges far longer than K_l_max + b_s)."""
+    cfg = get_config("tiny", S=6000, C=6000, H_q=8, H_kv=2, D=128, W=32, pool_k=7, K_l=200, recent=32,
+                     b_s=128, hh_frac=0.0, seed=60 + ctas)
+    inp = make_layer_inputs(cfg)
+    inp.k = inp.k[:, :, :1].expand_as(inp.k).contiguous()      # every key of a head is key 0
+    K_l, K_l_ref = U.kl_vector(cfg, K)
+    K.kvc_set_option(K.KVC_OPT_SCAN_CTAS, ctas)
+    try:
+        k_out, v_out, pos, off = U.run_compress(K, cfg, inp, K_l)
+    finally:
+        K.kvc_set_option(K.KVC_OPT_SCAN_CTAS, 0)
+    R = O.mandatory_set(cfg.S, cfg.sink, cfg.recent)
+    n_sel = cfg.K_l - len(R)
+    want = np.sort(np.concatenate([R, np.arange(cfg.sink, cfg.sink + n_sel)]))
+    for h in range(cfg.H_kv):
+        got = pos[off[h]:off[h + 1]].numpy()
+        assert np.array_equal(got, want), f"ctas={ctas} h={h}: kept {got[cfg.sink:cfg.sink + 8]}..."
+        o = U.oracle_head(cfg, inp, 0, h)
+        assert np.array_equal(O.select_topk(o["s"], cfg.K_l, cfg.sink, cfg.recent), want)
+        U.check_head_outputs(k_out, v_out, pos, off, inp, cfg, 0, h, K_l_ref[h], o["s"], f"all-equal ctas={ctas}")
+
+
+def test_padded_output_layout_matches_packed(K):
+    """A caller's own layout (out_off with room before and between heads):
+    select, gather and the whole compress fill the same rows as with the
+    packed layout, at the shifted places, and leave the other rows alone."""
+    cfg = small_cfg("gw160_qwen_like")            # B = 2, H_kv = 2
+    inp = make_layer_inputs(cfg)
+    K_l, _ = U.kl_vector(cfg, K)
+    K_l = [K_l[0], K_l[1] - 50]
+    k_ref, v_ref, p_ref, off = U.run_compress(K, cfg, inp, K_l)
+    lay = [5, 5 + K_l[0] + 11, 5 + K_l[0] + 11 + K_l[1] + 3]     # leading gap, gap between, gap at the end
+    T = lay[-1]
+    q, k, v = U.to_dev(inp)
+    ko = torch.full((cfg.B * T, cfg.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    vo = torch.full_like(ko, -7.0)
+    po = torch.full((cfg.B * T,), -5, dtype=torch.int32, device="cuda")
+    ws = K.workspace(cfg.B, cfg.H_q, cfg.H_kv, cfg.D, cfg.W, cfg.b_s, max(K_l), cfg.pool_k)
+    K.kvc_compress_layer(cfg.N, 0, cfg.B, cfg.S, cfg.C, cfg.H_q, cfg.H_kv, cfg.D, cfg.W, K_l, cfg.sink,
+                         cfg.recent, cfg.pool_k, cfg.b_s, q, k, v, ko, vo, po, ws, out_off=lay)
+    K.kvc_check_status()
+    ko, vo, po = ko.cpu(), vo.cpu(), po.cpu()
+    filled = np.zeros(cfg.B * T, dtype=bool)
+    for b in range(cfg.B):
+        for h in range(cfg.H_kv):
+            n = K_l[h]
+            a, r = b * T + lay[h], b * off[-1] + off[h]
+            filled[a:a + n] = True
+            assert torch.equal(po[a:a + n], p_ref[r:r + n]), f"b={b} h={h}: positions"
+            assert torch.equal(ko[a:a + n].view(torch.int16), k_ref[r:r + n].view(torch.int16))
+            assert torch.equal(vo[a:a + n].view(torch.int16), v_ref[r:r + n].view(torch.int16))
+    free = torch.from_numpy(~filled)
+    assert torch.all(po[free] == -5) and torch.all(ko[free] == 7.0) and torch.all(vo[free] == -7.0)
+    # the decomposed calls with the same layout
+    m = torch.empty((cfg.B, cfg.H_q, cfg.W), dtype=torch.float32, device="cuda")
+    Z = torch.empty_like(m)
+    K.kvc_score_pass1(q, k, cfg.B, cfg.H_q, cfg.H_kv, cfg.S, cfg.D, cfg.W, cfg.b_s, m, Z, ws)
+    sc = torch.empty((cfg.B, cfg.H_kv, cfg.S), dtype=torch.float32, device="cuda")
+    K.kvc_score_pass2_pool(q, k, m, Z, cfg.B, cfg.H_q, cfg.H_kv, cfg.S, cfg.D, cfg.W, cfg.b_s, cfg.pool_k, sc, ws)
+    idx = torch.full((cfg.B * T,), -9, dtype=torch.int32, device="cuda")
+    K.kvc_select_topk(sc, cfg.B, cfg.H_kv, cfg.S, K_l, cfg.sink, cfg.recent, idx, ws, out_off=lay)
+    k2 = torch.zeros((cfg.B * T, cfg.D), dtype=torch.bfloat16, device="cuda")
+    v2 = torch.zeros_like(k2)
+    p2 = torch.full((cfg.B * T,), -5, dtype=torch.int32, device="cuda")
+    K.kvc_gather(k, v, idx, cfg.B, cfg.H_kv, cfg.S, cfg.D, K_l, k2, v2, p2, out_off=lay)
+    K.kvc_check_status()
+    idx, p2 = idx.cpu(), p2.cpu()
+    assert torch.all(idx[free] == -9) and torch.all(p2[free] == -5)
+    for b in range(cfg.B):
+        for h in range(cfg.H_kv):
+            a = b * T + lay[h]
+            seg = p2[a:a + K_l[h]].numpy().astype(np.int64)
+            assert np.array_equal(idx[a:a + K_l[h]].numpy(), seg)
+            kh, vh, _ = O.gather(inp.k[b, h], inp.v[b, h], seg)
+            assert torch.equal(k2[a:a + K_l[h]].cpu().view(torch.int16), kh.view(torch.int16))

@@ -54,11 +54,30 @@ def _close(a, b):
     ("tiny", dict(B=2, S=3000, C=3000, H_q=10, H_kv=2, D=128, W=32, seed=7)),
 ])
 def test_noalloc_pass1_matches_workspace_pass1_twice(K, name, over):
+    """These shapes fit the default key-range plan, so both entry points run
+    the same kernels over the same ranges: m and Z must be bit-identical."""
     cfg = get_config(name, **over)
     inp = make_layer_inputs(cfg)
     q, k = inp.q_win.cuda(), inp.k.cuda()
     m_ref, Z_ref = _pass1_with_workspace(K, cfg, q, k)
     for call in range(2):                      # two calls in a row share the array
+        m, Z = _pass1_noalloc(K, cfg, q, k)
+        K.kvc_check_status()
+        assert torch.equal(m, m_ref), f"call {call}: m differs"
+        assert torch.equal(Z, Z_ref), f"call {call}: Z differs"
+
+
+def test_noalloc_pass1_one_range_per_head_plan(K):
+    """500 heads of 256 window rows: the default plan's partials (152 ranges,
+    each touching up to 4 heads: 1.2 MiB) do not fit the fixed array, so the
+    call falls back to one key range per head (1,024,000 bytes).  Different
+    ranges round differently, so the results agree within the scorer's
+    tolerance, on two calls in a row."""
+    cfg = get_config("tiny", B=125, H_q=32, H_kv=4, D=64, S=768, C=768, W=32, seed=11)
+    inp = make_layer_inputs(cfg)
+    q, k = inp.q_win.cuda(), inp.k.cuda()
+    m_ref, Z_ref = _pass1_with_workspace(K, cfg, q, k)
+    for call in range(2):
         m, Z = _pass1_noalloc(K, cfg, q, k)
         K.kvc_check_status()
         assert _close(m, m_ref), f"call {call}: m differs"
@@ -81,8 +100,17 @@ def test_noalloc_pass1_alternating_shapes(K):
 
 
 def test_noalloc_rejects_shapes_beyond_the_fixed_array(K):
-    # B * H_kv * roundup16(G*W) * 8 bytes = 1024 * 256 * 8 = 2 MiB > 1 MiB
+    # B * H_kv * roundup16(G*W) * 8 bytes = 1024 * 256 * 8 = 2 MiB > 1 MiB.
+    # The tensors are real and of the stated shapes, so that even a broken
+    # size check would only run a valid pass 1 (and fail the test), never
+    # read or write outside an allocation.
+    B, H_q, H_kv, S, D, W = 1024, 1, 1, 512, 64, 256
+    q = torch.zeros((B, H_q, W, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((B, H_kv, S, D), dtype=torch.bfloat16, device="cuda")
+    m = torch.zeros((B, H_q, W), dtype=torch.float32, device="cuda")
+    Z = torch.zeros_like(m)
     with pytest.raises(K.KvcError) as ei:
-        K.kvc_score_pass1_noalloc(16, 16, 1024, 1, 1, 512, 64, 256, 128, 16, 16)
+        K.kvc_score_pass1_noalloc(q, k, B, H_q, H_kv, S, D, W, 128, m, Z)
     assert ei.value.code == K.KVC_ERR_UNSUPPORTED
     assert "scratch" in str(ei.value)
+    K.kvc_check_status()
