@@ -45,6 +45,9 @@ def parse(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-full-layer", action="store_true",
+                    help="time the oracle on every KV head of layer 0 (a whole layer), whatever --cpu-seconds "
+                         "says; for multi-layer workloads the N-layer time is extrapolated linearly")
     ap.add_argument("--path", choices=["two_pass", "rawdot_int8", "append_chunk", "overlap"], default="two_pass",
                     help="two_pass: the layer compress (default, the headline); rawdot_int8: the single-pass "
                          "INT8 raw inner-product scorer, then the same selection and gather; append_chunk: the "
@@ -165,10 +168,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def oracle_sample(cfg, inp_cpu, heads, budget_s):
+NOMINAL_HBM_GBS = 7900.0   # HBM3e of one GB300, nominal
+
+
+def oracle_sample(cfg, inp_cpu, heads, budget_s, K_l):
     """Time the CPU oracle on whole KV heads of one layer (bounded sample)."""
     from oracle import kvc_oracle as O
-    K_l = [cfg.K_l if not cfg.inverse_stability else max(cfg.sink + cfg.recent, int(0.3 * cfg.S))] * cfg.H_kv
     keys, t_used, done = 0, 0.0, []
     for (b, h) in heads:
         t0 = time.perf_counter()
@@ -546,7 +551,8 @@ def main():
         except (ValueError, KeyError):
             traffic = None
     roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic, "peak_kind": peak_kind,
+                "frac": achieved / hbm_peak, "frac_of": f"the dominant kernel ({names[dom]}) alone",
+                "traffic": traffic, "peak_kind": peak_kind,
                 "alg_bytes_per_launch": alg[names[dom]], "ms_per_launch": per_launch_ms[dom]}
     stages = {n: round(t, 5) for n, t in zip(names, per_launch_ms)}
     path_gbs = path_bytes / (ms / args.steps / 1e3) / 1e9
@@ -631,10 +637,17 @@ def main():
         L0 = layers[0]
         heads = [(b, h) for b in range(cfg.B) for h in range(cfg.H_kv)]
         inp_cpu = {"q": L0["q"].cpu(), "k": L0["k"].cpu(), "v": L0["v"].cpu()}
-        v_cpu, t_cpu, done = oracle_sample(cfg, inp_cpu, heads, args.cpu_seconds)
+        budget_s = float("inf") if args.cpu_full_layer else args.cpu_seconds
+        v_cpu, t_cpu, done = oracle_sample(cfg, inp_cpu, heads, budget_s, L0["K_l"])
+        whole = len(done) == len(heads)
         cpu = {"value": v_cpu, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{len(done)} whole KV head(s) {done} of layer 0 ({cfg.S} keys each, dense fp64 "
-                         f"softmax over G*W={cfg.GW} rows), {t_cpu:.1f} s"}
+               "sample": (f"{'the whole layer: ' if whole else ''}{len(done)} KV head(s) of layer 0 "
+                          f"({cfg.S} keys each, dense fp64 softmax over G*W={cfg.GW} rows), {t_cpu:.1f} s")}
+        if whole:
+            cpu["layer_s"] = t_cpu
+            cpu["job_s"] = t_cpu * cfg.N
+            cpu["job_s_is"] = ("measured (one layer)" if cfg.N == 1 else
+                               f"extrapolated linearly from one measured layer to the {cfg.N} layers")
 
     if rank == 0:
         line = {
@@ -646,6 +659,7 @@ def main():
                              f"{2 * kbytes / 2**20:.0f} MiB K+V cycled"},
             "roofline": roofline,
             "path_hbm_gbs": path_gbs, "path_alg_bytes_per_step": path_bytes,
+            "path_frac_measured": path_gbs / hbm_peak, "path_frac_nominal": path_gbs / NOMINAL_HBM_GBS,
             "stage_ms_per_launch": stages,
             "gpu_launches": launches, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
         }
