@@ -20,6 +20,7 @@ __device__ int g_status_word;
 namespace {
 thread_local char t_err[512] = "";
 int64_t g_opt_scan_ctas = 0;
+int64_t g_opt_wait_limit = 0;
 std::mutex g_mu;
 int g_sms[64] = {0};
 int* g_status_ptr[64] = {nullptr};
@@ -84,6 +85,10 @@ int* status_word_ptr() {
     g_status_ptr[dev] = static_cast<int*>(p);
   }
   return g_status_ptr[dev];
+}
+
+uint32_t wait_limit_polls() {
+  return g_opt_wait_limit > 0 ? (uint32_t)std::min<int64_t>(g_opt_wait_limit, 1LL << 30) : (1u << 22);
 }
 
 int scan_ctas_target() {
@@ -341,6 +346,11 @@ int kvc_set_option(int option, int64_t value) {
   if (option == KVC_OPT_SCAN_CTAS) {
     if (value < 0) return set_error(KVC_ERR_INVALID_ARG, "scan CTA count must be >= 0");
     g_opt_scan_ctas = value;
+    return KVC_OK;
+  }
+  if (option == KVC_OPT_WAIT_LIMIT) {
+    if (value < 0) return set_error(KVC_ERR_INVALID_ARG, "wait limit must be >= 0");
+    g_opt_wait_limit = value;
     return KVC_OK;
   }
   return set_error(KVC_ERR_INVALID_ARG, "unknown option %d", option);

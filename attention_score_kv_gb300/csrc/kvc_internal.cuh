@@ -103,6 +103,7 @@ int check_ws(void* ws, size_t ws_bytes, size_t need);
 int cuda_error(cudaError_t e, const char* what);
 int num_sms();
 int scan_ctas_target();                             // SM count or the tuning override
+uint32_t wait_limit_polls();                        // polls before a pipeline wait gives up
 ScanPlan plan_for(int BH, int S, int P);            // exact plan for P CTAs
 ScanPlan make_plan(int BH, int S);                  // default plan
 int max_slots(int BH);                              // S-independent bound on plan slots

@@ -78,7 +78,7 @@ __device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, const Seg* segs, in
   uint32_t qphase = 0, u = 0, tcount = 0;
   for (int si = 0; si < nseg; ++si) {
     const Seg sg = segs[si];
-    if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) return;
+    if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status, A.wait_limit)) return;
     qphase ^= 1;
     const int ntiles = (sg.b - sg.a + kTile - 1) / kTile;
     for (int t = 0; t < ntiles; ++t, ++tcount) {
@@ -87,11 +87,12 @@ __device__ void mma_pass1(const ScanArgs& A, PipeBars* bars, const Seg* segs, in
       for (int mb = 0; mb < NMB; ++mb, ++u) {
         if ((int)(u & 1u) != who) continue;
         if (!mine) {
-          if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status)) return;
+          if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status, A.wait_limit)) return;
           mine = true;
         }
         const uint32_t b = u % kP1Bufs;
-        if (!wait_bar(smem_u32(&bars->tempty[b]), ((u / kP1Bufs) & 1u) ^ 1u, abort_flag, A.status)) return;
+        if (!wait_bar(smem_u32(&bars->tempty[b]), ((u / kP1Bufs) & 1u) ^ 1u, abort_flag, A.status, A.wait_limit))
+          return;
         tc::fence_after_sync();
         const uint32_t kb = sK + stage * kTileBytes;
 #pragma unroll
@@ -155,6 +156,7 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       Seg segs[kMaxSegs];
       const int nseg = cta_segments(A, blockIdx.x, segs);
       mma_pass1<D, NMB>(A, &bars, segs, nseg, sQ, sK, tmem, warp - 1, &s_abort);
+      drain_mma(smem_u32(&bars.drain[warp - 1]), A.status);   // its MMAs are done before TMEM is freed
     }
   } else {
     const int k = (warp - kFirstSmx) >> 2;     // 0..3
@@ -181,7 +183,7 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         const int t = p1_tile_order(ti, ntiles);
         const uint32_t u = (uint32_t)NMB * tcount + (uint32_t)mb;   // this warp's sub-tile
         const uint32_t buf = u % kP1Bufs;
-        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), (u / kP1Bufs) & 1u, &s_abort, A.status)) { ok = false; break; }
+        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), (u / kP1Bufs) & 1u, &s_abort, A.status, A.wait_limit)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t taddr = tmem + buf * 128 + col0 + ((uint32_t)(quarter * 32) << 16);
         // Every warp loads, active or not (a load under a runtime condition

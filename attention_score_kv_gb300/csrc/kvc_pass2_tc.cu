@@ -160,7 +160,7 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
     const Seg sg = segs[s];
     int okl = 1;
     if (s > 0) {
-      if (lane == 0) okl = wait_bar(smem_u32(&rb->bias_free), bphase, abort_flag, A.status);
+      if (lane == 0) okl = wait_bar(smem_u32(&rb->bias_free), bphase, abort_flag, A.status, A.wait_limit);
       bphase ^= 1;
     }
     if (!__shfl_sync(0xffffffffu, okl, 0)) return;
@@ -192,12 +192,12 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
     tc::fence_proxy_async();
     __syncwarp();
     if (lane == 0) {
-      if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status)) okl = 0;
+      if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status, A.wait_limit)) okl = 0;
       qphase ^= 1;
       const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
       for (int t = 0; t < ntiles && okl; ++t) {
-        if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status) ||
-            !wait_bar(smem_u32(&bars->tempty[buf]), tphase ^ 1, abort_flag, A.status)) {
+        if (!wait_bar(smem_u32(&bars->full[stage]), phase, abort_flag, A.status, A.wait_limit) ||
+            !wait_bar(smem_u32(&bars->tempty[buf]), tphase ^ 1, abort_flag, A.status, A.wait_limit)) {
           okl = 0;
           break;
         }
@@ -282,6 +282,7 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
     }
   } else if (warp == 1) {
     mma_warp<D>(A, &bars, &rbars, segs, nseg, sQ, sK, sOnes, sBias, tmem, &s_abort);
+    if (lane == 0) drain_mma(smem_u32(&bars.drain[0]), A.status);   // its MMAs are done before TMEM is freed
   } else if (warp < kPoolWarp) {
     // ---------------------------------------------------- softmax warps
     // Warp k of a lane quarter owns column chunks [k*cw, k*cw + cw) of the
@@ -306,7 +307,8 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       for (int it = 0; it < n_iter; ++it, ++tcount) {
         const int t0 = sg.a - hw + it * kTile;
         const uint32_t buf = (uint32_t)tcount & 1u;
-        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), ((uint32_t)tcount >> 1) & 1u, &s_abort, A.status)) {
+        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), ((uint32_t)tcount >> 1) & 1u, &s_abort, A.status,
+                           A.wait_limit)) {
           ok = false;
           break;
         }
@@ -360,7 +362,8 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         }
         const float r = (a0.x + a0.y) + (a1.x + a1.y) + ((a2.x + a2.y) + (a3.x + a3.y));
         const int slot = tcount % kRing;
-        if (!wait_bar_warp(smem_u32(&rbars.rempty[slot]), ((tcount / kRing) & 1) ^ 1, &s_abort, A.status)) {
+        if (!wait_bar_warp(smem_u32(&rbars.rempty[slot]), ((tcount / kRing) & 1) ^ 1, &s_abort, A.status,
+                           A.wait_limit)) {
           ok = false;
           break;
         }
@@ -391,7 +394,7 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
           if (lane < kRingPad) rr[lane] = 0.f;   // keys before the segment's first tile: none
           __syncwarp();
         }
-        if (!wait_bar_warp(smem_u32(&rbars.rfull[slot]), (tcount / kRing) & 1, &s_abort, A.status)) { ok = false; break; }
+        if (!wait_bar_warp(smem_u32(&rbars.rfull[slot]), (tcount / kRing) & 1, &s_abort, A.status, A.wait_limit)) { ok = false; break; }
         {
           // key mass = the sum of its four slice sums; keys outside [0, S) weigh nothing
           const int jb = t0 + 4 * lane;

@@ -97,15 +97,20 @@ kvc_rawdot_score_kernel(const __nv_bfloat16* __restrict__ k, int64_t rows, int64
   const uint32_t base = smem_u32(ring);
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t st = 0, ph = 0;
+      uint32_t st = 0, ph = 0, loaded = 0, last_par = 0;
       for (int t = 0; t < nchunks; ++t) {
         if (!scan::wait_bar(smem_u32(&empty[st]), ph ^ 1u, &s_abort, status)) break;
         const int64_t r = r_a + (int64_t)t * kRingRows;
         const uint32_t bytes = (uint32_t)(min((int64_t)kRingRows, r_b - r) * ROWB);
         tc::mbar_arrive_expect_tx(smem_u32(&full[st]), bytes);
         tc::bulk_g2s(base + st * kStageBytes, k + (size_t)r * D, bytes, smem_u32(&full[st]));
+        loaded |= 1u << st;
+        last_par = (last_par & ~(1u << st)) | (ph << st);
         if (++st == kRingStages) { st = 0; ph ^= 1u; }
       }
+      // every copy issued has landed before this thread may leave the CTA
+      for (int s = 0; s < kRingStages; ++s)
+        if (loaded & (1u << s)) scan::drain_wait(smem_u32(&full[s]), (last_par >> s) & 1u, status);
     }
     return;
   }

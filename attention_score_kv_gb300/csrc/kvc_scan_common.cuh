@@ -37,12 +37,14 @@ constexpr int kStages = KVC_P1_STAGES;        // key-tile ring depth of pass 1
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccStride = 256;          // TMEM columns per accumulator buffer
-constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up
+constexpr uint32_t kWaitLimit = 1u << 22;     // polls before a wait gives up (default)
+constexpr uint32_t kDrainLimit = 1u << 26;    // polls while draining copies / MMAs already issued
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSegs = 8;
 
 struct ScanArgs {
   int B, H_q, H_kv, S, W, gw, gwp16, n_mb, nq, P, maxseg, pool_k, cap;
+  uint32_t wait_limit;       // polls before a pipeline wait gives up
   int inputs_ready;          // pass 2: keys and queries were complete before the previous grid ran
   int64_t L;
   float c2;                  // log2(e) / sqrt(D)
@@ -64,8 +66,9 @@ struct Seg {
 };
 
 // Bounded wait; on giving up, flags the CTA and the status word.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                         uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     if ((i & 4095u) == 4095u && *abort_flag) return false;
   }
@@ -78,15 +81,33 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // instruction, so the warp never diverges: a barrier that is already
 // complete costs one read (about 20 cycles), where one polling lane plus a
 // broadcast costs over 300 (the warp splits and reconverges around the poll).
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                              uint32_t limit = kWaitLimit) {
   if (tc::mbar_try_wait(bar, parity)) return true;
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     if ((i & 4095u) == 4095u && *abort_flag) return false;
   }
   *abort_flag = 1;
   if ((threadIdx.x & 31) == 0) record_status(status, kStatusTimeout);
   return false;
+}
+
+// Draining before a CTA leaves.  Copies and MMAs a CTA has issued always
+// complete, whether or not a wait gave up meanwhile; shared and tensor memory
+// must not be released before they have.  So every thread that issued them
+// waits for their completion barriers first, with a limit far above any
+// completion time (the pipeline waits above may have been given a short
+// one).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  for (uint32_t i = 0; i < kDrainLimit; ++i)
+    if (tc::mbar_try_wait(bar, parity)) return;
+  record_status(status, kStatusTimeout);
+}
+// All MMAs (and tensor-memory copies) issued so far by this thread.
+__device__ __forceinline__ void drain_mma(uint32_t bar, int* status) {
+  tc::mma_commit(bar);
+  drain_wait(bar, 0, status);
 }
 
 // Pass-1 tile order within a segment: the leading third of the keys comes
@@ -135,7 +156,7 @@ __device__ __forceinline__ float2 combine_partials(const ScanArgs& A, int bh, in
 }
 
 struct PipeBars {
-  uint64_t full[kMaxStages], empty[kMaxStages], tfull[4], tempty[4], qfull, qempty;
+  uint64_t full[kMaxStages], empty[kMaxStages], tfull[4], tempty[4], qfull, qempty, drain[2];
 };
 
 // empty_count / qempty_count: commits that free a ring stage / the queries
@@ -152,6 +173,8 @@ __device__ __forceinline__ void init_pipe_bars(PipeBars* b, int tempty_count, in
   }
   tc::mbar_init(smem_u32(&b->qfull), 1);
   tc::mbar_init(smem_u32(&b->qempty), qempty_count);
+  tc::mbar_init(smem_u32(&b->drain[0]), 1);
+  tc::mbar_init(smem_u32(&b->drain[1]), 1);
 }
 
 // TMA producer (one thread): per segment the window queries, then the key
@@ -169,10 +192,12 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
   const int G = A.H_q / A.H_kv;
   const uint64_t k_policy = PASS == 2 ? tc::l2_evict_first_policy() : 0ull;
   uint32_t stage = 0, phase = 0, qphase = 0;
-  for (int si = 0; si < nseg; ++si) {
+  uint32_t loaded = 0, last_par = 0;   // per stage: ever loaded / parity of its last load (bit masks)
+  bool q_loaded = false, ok = true;
+  for (int si = 0; si < nseg && ok; ++si) {
     const Seg sg = segs[si];
     if (si > 0) {
-      if (!wait_bar(smem_u32(&bars->qempty), qphase, abort_flag, A.status)) return;
+      if (!wait_bar(smem_u32(&bars->qempty), qphase, abort_flag, A.status, A.wait_limit)) break;
       qphase ^= 1;
     }
     const int b_idx = sg.bh / A.H_kv, hk = sg.bh % A.H_kv;
@@ -180,11 +205,15 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
     tc::mbar_arrive_expect_tx(smem_u32(&bars->qfull), q_bytes);
     for (int kh = 0; kh < NKH; ++kh)
       tc::tma_load_3d(sQ + kh * q_half, qmap, smem_u32(&bars->qfull), kh * 64, qrow, 0);
+    q_loaded = true;
     const int start = sg.a - hw;
     const int ntiles = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
     for (int ti = 0; ti < ntiles; ++ti) {
       const int t = PASS == 1 ? p1_tile_order(ti, ntiles) : ti;
-      if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, A.status)) return;
+      if (!wait_bar(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, A.status, A.wait_limit)) {
+        ok = false;
+        break;
+      }
       const uint32_t dst = sK + stage * kTileBytes;
       tc::mbar_arrive_expect_tx(smem_u32(&bars->full[stage]), kTileBytes);
       for (int kh = 0; kh < NKH; ++kh) {
@@ -195,9 +224,15 @@ __device__ void producer(const ScanArgs& A, const CUtensorMap* qmap, const CUten
           tc::tma_load_3d(dst + kh * (kTile * 128), kmap, smem_u32(&bars->full[stage]), kh * 64, start + t * kTile,
                           sg.bh);
       }
+      loaded |= 1u << stage;
+      last_par = (last_par & ~(1u << stage)) | (phase << stage);
       if (++stage == NST) { stage = 0; phase ^= 1; }
     }
   }
+  // every copy issued has landed before the CTA may leave
+  for (int st = 0; st < NST; ++st)
+    if (loaded & (1u << st)) drain_wait(smem_u32(&bars->full[st]), (last_par >> st) & 1u, A.status);
+  if (q_loaded) drain_wait(smem_u32(&bars->qfull), qphase, A.status);
 }
 
 // ------------------------------------------------------------- host side
@@ -246,6 +281,7 @@ inline ScanArgs base_args(const ScanPlan& pl, int B, int H_q, int H_kv, int S, i
   A.maxseg = pl.maxseg;
   A.c2 = kLog2e / sqrtf((float)D);
   A.status = status_word_ptr();
+  A.wait_limit = wait_limit_polls();
   A.pool_k = 1;
   return A;
 }

@@ -27,6 +27,7 @@ KVC_ERR_CUDA = -4
 KVC_ERR_TIMEOUT = -5
 KVC_ERR_DEVICE = -6
 KVC_OPT_SCAN_CTAS = 1
+KVC_OPT_WAIT_LIMIT = 2
 
 _NAMES = {
     KVC_ERR_INVALID_ARG: "invalid argument", KVC_ERR_UNSUPPORTED: "unsupported",

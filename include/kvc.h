@@ -354,7 +354,12 @@ int kvc_check_status(kvc_stream_t stream);
 
 /* Tuning knobs (process-wide, not thread-safe; 0 restores the default). */
 enum kvc_option {
-  KVC_OPT_SCAN_CTAS = 1  /* CTAs (key ranges) of the two scans; default: the SM count */
+  KVC_OPT_SCAN_CTAS = 1,  /* CTAs (key ranges) of the two scans; default: the SM count */
+  KVC_OPT_WAIT_LIMIT = 2  /* polls before a wait inside a scan pipeline gives up and the
+                             call ends with KVC_ERR_TIMEOUT (kvc_check_status); default
+                             2^22.  A wait that gives up stops the CTA's pipeline; the
+                             copies and MMAs it already issued are waited for before the
+                             CTA leaves.  Results of such a call are undefined. */
 };
 int kvc_set_option(int option, int64_t value);
 
