@@ -618,6 +618,45 @@ int kvc_head_similarity(const int32_t* idx, const int64_t* off, int n_groups, in
                        "similarity launch");
 }
 
+static int check_steps(int T, int H) {
+  if (T < 1 || H < 1) return set_error(KVC_ERR_INVALID_ARG, "T and H must be >= 1");
+  if (T > kMaxDecodeSteps) return set_error(KVC_ERR_UNSUPPORTED, "T=%d above %d steps", T, kMaxDecodeSteps);
+  if (H > 65535) return set_error(KVC_ERR_UNSUPPORTED, "H=%d above 65535", H);
+  return KVC_OK;
+}
+
+int kvc_median_over_steps(const float* x, int T, int H, float* med, kvc_stream_t stream) {
+  int rc;
+  if ((rc = check_steps(T, H)) || (rc = check_ptr(x, 4, "x")) || (rc = check_ptr(med, 4, "med"))) return rc;
+  return launch_status(launch_median(x, T, H, med, reinterpret_cast<cudaStream_t>(stream)), "median launch");
+}
+
+int kvc_head_stability_over_steps(const int32_t* dec_idx, const int64_t* dec_off, const int32_t* pre_idx,
+                                  const int64_t* pre_off, int T, int H, float* per_step, float* stability,
+                                  kvc_stream_t stream) {
+  int rc;
+  if ((rc = check_steps(T, H)) || (rc = check_ptr(dec_idx, 4, "dec_idx")) || (rc = check_ptr(dec_off, 8, "dec_off")) ||
+      (rc = check_ptr(pre_idx, 4, "pre_idx")) || (rc = check_ptr(pre_off, 8, "pre_off")) ||
+      (rc = check_ptr(per_step, 4, "per_step")) || (rc = check_ptr(stability, 4, "stability")))
+    return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = launch_status(launch_stability_steps(dec_idx, dec_off, pre_idx, pre_off, T, H, per_step, st),
+                          "stability overlap launch")))
+    return rc;
+  return launch_status(launch_median(per_step, T, H, stability, st), "median launch");
+}
+
+int kvc_head_similarity_over_steps(const int32_t* idx, const int64_t* off, int T, int H, float* per_step,
+                                   float* similarity, kvc_stream_t stream) {
+  int rc;
+  if ((rc = check_steps(T, H)) || (rc = check_ptr(idx, 4, "idx")) || (rc = check_ptr(off, 8, "off")) ||
+      (rc = check_ptr(per_step, 4, "per_step")) || (rc = check_ptr(similarity, 4, "similarity")))
+    return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = launch_status(launch_similarity(idx, off, T, H, per_step, st), "similarity launch"))) return rc;
+  return launch_status(launch_median(per_step, T, H, similarity, st), "median launch");
+}
+
 int kvc_budget_inverse_stability_device(int n_layers, int H_kv, const double* s_stable, int64_t total, int lo,
                                         int hi, int32_t* K_l_out, kvc_stream_t stream) {
   int rc;

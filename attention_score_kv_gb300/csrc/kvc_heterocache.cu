@@ -21,6 +21,7 @@ namespace kvc {
 namespace {
 
 constexpr int kOvThreads = 256;
+constexpr int kMaxSteps = kMaxDecodeSteps;
 
 // Hits of the shorter list in the longer one, summed over the CTA.
 __device__ int intersect_count(const int32_t* a, int na, const int32_t* b, int nb, int* scratch) {
@@ -78,6 +79,56 @@ kvc_similarity_kernel(const int32_t* __restrict__ idx, const int64_t* __restrict
     best = fmaxf(best, overlap_of(inter, ni, nj));
   }
   if (threadIdx.x == 0) sim[(size_t)g * H + i] = H > 1 ? best : 0.f;
+}
+
+// Phase 1 over decoding steps.  One CTA per (head h, step t): the overlap of
+// the head's top-k at step t with its prefill set, into per_step[t][h].
+__global__ void __launch_bounds__(kOvThreads)
+kvc_stability_step_kernel(const int32_t* __restrict__ dec_idx, const int64_t* __restrict__ dec_off,
+                          const int32_t* __restrict__ pre_idx, const int64_t* __restrict__ pre_off, int H,
+                          float* __restrict__ per_step) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ int scratch[32];
+  const int h = blockIdx.x, t = blockIdx.y;
+  const size_t d = (size_t)t * H + h;
+  const int nd = (int)(dec_off[d + 1] - dec_off[d]), np_ = (int)(pre_off[h + 1] - pre_off[h]);
+  const int inter = intersect_count(dec_idx + dec_off[d], nd, pre_idx + pre_off[h], np_, scratch);
+  if (threadIdx.x == 0) per_step[d] = overlap_of(inter, nd, np_);
+}
+
+// One CTA per head: the median over T steps of x[t][h].  Order statistics by
+// rank counting (value v holds ranks #{x < v} .. #{x <= v} - 1); for odd T
+// the middle one, for even T the two middle ones averaged exactly in fp64
+// and rounded once to fp32.  -0 counts as +0; NaN inputs give NaN.
+__global__ void __launch_bounds__(kOvThreads)
+kvc_median_kernel(const float* __restrict__ x, int T, int H, float* __restrict__ out) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ float v[kMaxSteps];
+  __shared__ float s_lo, s_hi;
+  const int h = blockIdx.x;
+  if (threadIdx.x == 0) {
+    s_lo = __int_as_float(0x7fc00000);
+    s_hi = s_lo;
+  }
+  for (int t = threadIdx.x; t < T; t += blockDim.x) v[t] = x[(size_t)t * H + h] + 0.0f;
+  __syncthreads();
+  const int k_lo = (T - 1) / 2, k_hi = T / 2;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const float a = v[t];
+    int lt = 0, le = 0;
+    for (int u = 0; u < T; ++u) {
+      lt += v[u] < a ? 1 : 0;
+      le += v[u] <= a ? 1 : 0;
+    }
+    // threads holding equal values write the same value
+    if (lt <= k_lo && k_lo < le) s_lo = a;
+    if (lt <= k_hi && k_hi < le) s_hi = a;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    out[h] = (T & 1) ? s_lo : __double2float_rn(((double)s_lo + (double)s_hi) * 0.5);
 }
 
 // One CTA per layer, one thread per head.
@@ -144,6 +195,20 @@ cudaError_t launch_overlap(const int32_t* a, const int64_t* a_off, const int32_t
 cudaError_t launch_similarity(const int32_t* idx, const int64_t* off, int n_groups, int H, float* sim,
                               cudaStream_t st) {
   cudaError_t e = launch_pdl(kvc_similarity_kernel, dim3(H, n_groups), dim3(kOvThreads), 0, st, idx, off, H, sim);
+  note_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_stability_steps(const int32_t* dec_idx, const int64_t* dec_off, const int32_t* pre_idx,
+                                   const int64_t* pre_off, int T, int H, float* per_step, cudaStream_t st) {
+  cudaError_t e = launch_pdl(kvc_stability_step_kernel, dim3(H, T), dim3(kOvThreads), 0, st, dec_idx, dec_off, pre_idx,
+                             pre_off, H, per_step);
+  note_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_median(const float* x, int T, int H, float* out, cudaStream_t st) {
+  cudaError_t e = launch_pdl(kvc_median_kernel, dim3(H), dim3(kOvThreads), 0, st, x, T, H, out);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -16,6 +16,7 @@ constexpr int kMaxGWP = 256;        // G*W rounded up to 16
 constexpr int kMaxPool = 15;        // widest average pool
 constexpr int kMaxSeg = 8;          // KV heads one scan CTA may touch
 constexpr int kMinKeysPerCta = 1024;
+constexpr int kMaxDecodeSteps = 4096;  // decoding steps a Phase-1 median runs over
 constexpr int kHist1 = 2048;        // radix digits: bits 31..21, 20..10, 9..0 of the score
 constexpr int kHist2 = 2048;
 constexpr int kHist3 = 1024;
@@ -165,6 +166,10 @@ cudaError_t launch_overlap(const int32_t* a, const int64_t* a_off, const int32_t
                            int n_pairs, float* out, cudaStream_t st);
 cudaError_t launch_similarity(const int32_t* idx, const int64_t* off, int n_groups, int H, float* sim,
                               cudaStream_t st);
+// Phase 1 over decoding steps: per-step stability overlaps, medians over steps
+cudaError_t launch_stability_steps(const int32_t* dec_idx, const int64_t* dec_off, const int32_t* pre_idx,
+                                   const int64_t* pre_off, int T, int H, float* per_step, cudaStream_t st);
+cudaError_t launch_median(const float* x, int T, int H, float* out, cudaStream_t st);
 cudaError_t launch_budget(const double* s_stable, int n_layers, int H, int64_t total, int lo, int hi,
                           int32_t* K_l, cudaStream_t st);
 // selection over dense scores (mode 0) or candidate lists (mode 1)

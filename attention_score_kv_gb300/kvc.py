@@ -73,6 +73,9 @@ _SIGS = {
     "kvc_overlap_coefficient": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "kvc_head_similarity": (_I, [_P, _P, _I, _I, _P, _P]),
     "kvc_budget_inverse_stability_device": (_I, [_I, _I, _P, _I64, _I, _I, _P, _P]),
+    "kvc_median_over_steps": (_I, [_P, _I, _I, _P, _P]),
+    "kvc_head_stability_over_steps": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P]),
+    "kvc_head_similarity_over_steps": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "kvc_append_chunk": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "kvc_cache_layout": (_I, [_I, _I, _I, _I, _I32P, _I64P]),
     "kvc_scan_ranges": (_I, [_I, _I, _I, _I64P]),
@@ -193,6 +196,20 @@ def kvc_overlap_coefficient(a, a_off, b, b_off, n_pairs, out, stream=None):
 
 def kvc_head_similarity(idx, off, n_groups, H, sim, stream=None):
     _check(_lib.kvc_head_similarity(_ptr(idx), _ptr(off), n_groups, H, _ptr(sim), _stream(stream)))
+
+
+def kvc_median_over_steps(x, T, H, med, stream=None):
+    _check(_lib.kvc_median_over_steps(_ptr(x), T, H, _ptr(med), _stream(stream)))
+
+
+def kvc_head_stability_over_steps(dec_idx, dec_off, pre_idx, pre_off, T, H, per_step, stability, stream=None):
+    _check(_lib.kvc_head_stability_over_steps(_ptr(dec_idx), _ptr(dec_off), _ptr(pre_idx), _ptr(pre_off), T, H,
+                                              _ptr(per_step), _ptr(stability), _stream(stream)))
+
+
+def kvc_head_similarity_over_steps(idx, off, T, H, per_step, similarity, stream=None):
+    _check(_lib.kvc_head_similarity_over_steps(_ptr(idx), _ptr(off), T, H, _ptr(per_step), _ptr(similarity),
+                                               _stream(stream)))
 
 
 def kvc_budget_inverse_stability_device(n_layers, H_kv, s_stable, total, lo, hi, K_l_out, stream=None):

@@ -267,6 +267,50 @@ int kvc_head_similarity(const int32_t* idx, const int64_t* off, int n_groups,
                         int H, float* sim, kvc_stream_t stream);
 
 /*
+ * HeteroCache's Phase-1 scores over decoding steps (HeteroCache summary,
+ * "Methodology", Phase 1): the stability score of a head is the median over
+ * T decoding steps of the overlap coefficient between its top-k at that
+ * step and its prefill set; the similarity score is the median over the
+ * same steps of the largest overlap with another head of its layer.  Median
+ * of T fp32 values: the middle one for odd T; for even T the two middle
+ * ones averaged exactly (fp64) and rounded once to fp32; -0 counts as +0,
+ * NaN gives NaN.  1 <= T <= 4096 (else KVC_ERR_UNSUPPORTED), 1 <= H <= 65535.
+ *
+ * kvc_median_over_steps: x fp32 [T][H], device -> med fp32 [H], device.
+ */
+int kvc_median_over_steps(const float* x, int T, int H, float* med,
+                          kvc_stream_t stream);
+
+/*
+ *   dec_idx, dec_off  the decoding-step sets: set (t, h) is
+ *                     dec_idx[dec_off[t*H + h] .. dec_off[t*H + h + 1] - 1]
+ *                     (dec_off int64 [T*H + 1]); sets ascending, no
+ *                     duplicates, as kvc_select_topk writes them
+ *   pre_idx, pre_off  the prefill sets of the H heads (pre_off [H + 1])
+ *   per_step          fp32 [T][H] out: the per-step overlaps (also the
+ *                     scratch of the median; the caller owns it)
+ *   stability         fp32 [H] out
+ * All device pointers.
+ */
+int kvc_head_stability_over_steps(const int32_t* dec_idx,
+                                  const int64_t* dec_off,
+                                  const int32_t* pre_idx,
+                                  const int64_t* pre_off, int T, int H,
+                                  float* per_step, float* stability,
+                                  kvc_stream_t stream);
+
+/*
+ *   idx, off    step t's H sets, as kvc_head_similarity's groups: set (t, h)
+ *               is idx[off[t][h] .. off[t][h+1] - 1], off int64 [T][H + 1]
+ *   per_step    fp32 [T][H] out: each step's largest overlap per head
+ *   similarity  fp32 [H] out
+ * All device pointers.
+ */
+int kvc_head_similarity_over_steps(const int32_t* idx, const int64_t* off,
+                                   int T, int H, float* per_step,
+                                   float* similarity, kvc_stream_t stream);
+
+/*
  * kvc_budget_inverse_stability on the device, for n_layers layers at once
  * (HeteroCache, Phase 2): the same float64 operations in the same order, so
  * the budgets equal the host function's.

@@ -85,3 +85,61 @@ def test_device_budgets_equal_host_and_oracle(K):
     for l in range(n_layers):
         assert got[l].tolist() == K.kvc_budget_inverse_stability(s[l], total, lo, hi), l
         assert got[l].tolist() == O.budgets_inverse_stability(s[l], total, lo, hi).tolist(), l
+
+
+def _drifting_sets(rng, T, H, S, k, drift):
+    """Seeded synthetic decoding-step top-k sets: each head starts from its
+    prefill set and replaces a head-specific share of it at every step."""
+    pre = [np.sort(rng.choice(S, k, replace=False)) for _ in range(H)]
+    dec = []
+    for t in range(T):
+        row = []
+        for h in range(H):
+            keep = rng.random(k) >= drift[h]
+            new = rng.choice(S, int((~keep).sum()), replace=False)
+            row.append(np.unique(np.concatenate([pre[h][keep], new])))
+        dec.append(row)
+    return pre, dec
+
+
+@pytest.mark.parametrize("T", [1, 100, 101])
+def test_phase1_medians_over_steps_bit_exact(K, T):
+    """HeteroCache Phase 1: stability = median over T steps of the overlap of
+    each head's step set with its prefill set; similarity = median over the
+    steps of the per-step maximum overlap with another head."""
+    rng = np.random.default_rng(T)
+    H, S, k = 8, 32768, 512
+    drift = np.linspace(0.02, 0.9, H)
+    pre, dec = _drifting_sets(rng, T, H, S, k, drift)
+    flat_dec = [dec[t][h] for t in range(T) for h in range(H)]
+    d_idx, d_off = _csr(flat_dec)
+    p_idx, p_off = _csr(pre)
+    per = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    stab = torch.empty(H, dtype=torch.float32, device="cuda")
+    K.kvc_head_stability_over_steps(d_idx, d_off, p_idx, p_off, T, H, per, stab)
+    # similarity: each step a group of H sets with its own CSR offsets
+    offs = [np.concatenate([[0], np.cumsum([len(x) for x in dec[t]])]) for t in range(T)]
+    base = np.cumsum([0] + [o[-1] for o in offs[:-1]])
+    off2 = torch.from_numpy(np.stack([o + b for o, b in zip(offs, base)]).astype(np.int64)).cuda()
+    per2 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    sim = torch.empty(H, dtype=torch.float32, device="cuda")
+    K.kvc_head_similarity_over_steps(d_idx, off2, T, H, per2, sim)
+    K.kvc_check_status()
+    ref_per, ref_stab = Hc.stability_over_steps(dec, pre)
+    ref_per2, ref_sim = Hc.similarity_over_steps(dec)
+    assert np.array_equal(per.cpu().numpy().view(np.uint32), ref_per.view(np.uint32))
+    assert np.array_equal(stab.cpu().numpy().view(np.uint32), ref_stab.view(np.uint32))
+    assert np.array_equal(per2.cpu().numpy().view(np.uint32), ref_per2.view(np.uint32))
+    assert np.array_equal(sim.cpu().numpy().view(np.uint32), ref_sim.view(np.uint32))
+    if T > 1:   # slow drift gives the higher stability
+        assert np.all(np.diff(ref_stab) <= 0)
+
+
+def test_median_over_steps_ties_and_signs(K):
+    x = np.array([[0.25, -0.0, 1.0], [0.25, 0.0, 2.0], [0.5, -0.0, 3.0], [0.75, 5.0, 4.0]], dtype=np.float32)
+    for T in (1, 2, 3, 4):
+        med = torch.empty(3, dtype=torch.float32, device="cuda")
+        K.kvc_median_over_steps(torch.from_numpy(x[:T].copy()).cuda(), T, 3, med)
+        K.kvc_check_status()
+        ref = Hc.median_over_steps(x[:T])
+        assert np.array_equal(med.cpu().numpy().view(np.uint32), ref.view(np.uint32)), T
