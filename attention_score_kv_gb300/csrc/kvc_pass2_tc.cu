@@ -28,18 +28,32 @@ namespace {
 
 using namespace scan;
 
-constexpr int kStages2 = 3;
+constexpr int kStages2 = 4;
+// The bias K-step's operands (16 K elements a row) in the unswizzled
+// core-matrix layout: row r of a block at (r/8)*256 + (r%8)*16 for K
+// elements 0-7, +128 for 8-15, so a row takes 32 bytes instead of a
+// 128-byte swizzled row.
+constexpr uint32_t kOnesBytes = kTile * 32;
+constexpr uint32_t kBiasBytes = kMaxGWP * 32;
+constexpr uint32_t kBiasLbo = 128, kBiasSbo = 256;
 constexpr int kSmxWarps = 16;                    // four per TMEM lane quarter
 constexpr int kSlices = kSmxWarps / 4;           // column slices of a tile
-constexpr int kPoolWarp = 2 + kSmxWarps;         // warp 18
-constexpr int kThreads = 32 * (kPoolWarp + 1);
+constexpr int kPoolWarp = 2 + kSmxWarps;         // warps 18 and 19 pool alternate tiles
+constexpr int kThreads = 32 * (kPoolWarp + 2);
 constexpr int kRing = 4;
 constexpr int kRingPad = 16;                     // room for the previous tile's last 2h masses
 static_assert(kMaxPool - 1 <= kRingPad, "the pooling halo must fit the ring pad");
 constexpr float kNoWeight = -1.0e30f;            // bias of padding rows: weight 0
 
 struct RingBars {
-  uint64_t rfull[kRing], rempty[kRing], bias_free;
+  uint64_t rfull[kRing], rempty[kRing], mass[kRing], hand[2], bias_free;
+};
+
+// State of a segment's candidate list, handed from the pooling warp of one
+// tile to the pooling warp of the next.
+struct ListHand {
+  int cnt;
+  long long tau;
 };
 
 struct WarpCompact {
@@ -142,19 +156,18 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
   const uint32_t q_half = (uint32_t)A.nq * 128;
   const int hw = (A.pool_k - 1) / 2;
   const uint32_t idesc = tc::idesc_bf16(128, A.gwp16);
-  // key side of the bias K-step: row r, K elements 0..2 = 1.0, the rest 0
-  // (128-byte swizzle: logical 16-byte chunk c of row r sits at chunk c ^ (r & 7))
-  for (int idx = lane; idx < kTile * 8; idx += 32) {
-    const int row = idx >> 3, pch = idx & 7;
-    const bool first = (pch ^ (row & 7)) == 0;
+  // key side of the bias K-step: row r, K elements 0..2 = 1.0, the rest 0;
+  // 16-byte unit i holds row 8*(i/16) + i%8, K elements 8*((i/8)%2) .. +7
+  for (int i = lane; i < (int)(kOnesBytes / 16); i += 32) {
+    const bool first = ((i >> 3) & 1) == 0;
     const uint4 val = first ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(sOnes + idx * 16), "r"(val.x), "r"(val.y),
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(sOnes + i * 16), "r"(val.x), "r"(val.y),
                  "r"(val.z), "r"(val.w)
                  : "memory");
   }
-  // query side: only logical chunk 0 of each row ever holds data
-  for (int idx = lane; idx < A.nq * 8; idx += 32)
-    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(sBias + idx * 16), "r"(0u) : "memory");
+  // query side: only K elements 0..2 of each row ever hold data
+  for (int i = lane; i < A.nq * 2; i += 32)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(sBias + i * 16), "r"(0u) : "memory");
   uint32_t stage = 0, phase = 0, qphase = 0, buf = 0, tphase = 0, bphase = 0;
   for (int s = 0; s < nseg; ++s) {
     const Seg sg = segs[s];
@@ -183,9 +196,8 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
         const float r2 = r1 - __bfloat162float(mid);
         const uint32_t x = bf16_bits(__bfloat162float(hi)) | (bf16_bits(__bfloat162float(mid)) << 16);
         const uint32_t y = bf16_bits(r2);
-        // logical chunk 0 of row `row` sits at physical chunk (row & 7)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %3};\n" ::"r"(sBias + row * 128 + (row & 7) * 16), "r"(x),
-                     "r"(y), "r"(0u)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %3};\n" ::"r"(sBias + (row >> 3) * kBiasSbo + (row & 7) * 16),
+                     "r"(x), "r"(y), "r"(0u)
                      : "memory");
       }
     }
@@ -210,7 +222,7 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
           const uint32_t qoff = (ks >> 2) * q_half + (ks & 3) * 32;
           tc::mma_bf16(dacc, tc::desc_sw128(kb + koff), tc::desc_sw128(sQ + qoff), idesc, ks > 0);
         }
-        tc::mma_bf16(dacc, tc::desc_sw128(sOnes), tc::desc_sw128(sBias), idesc, 1);
+        tc::mma_bf16(dacc, tc::desc_nosw(sOnes, kBiasLbo, kBiasSbo), tc::desc_nosw(sBias, kBiasLbo, kBiasSbo), idesc, 1);
         tc::mma_commit(smem_u32(&bars->empty[stage]));
         tc::mma_commit(smem_u32(&bars->tfull[buf]));
         if (++stage == kStages2) { stage = 0; phase ^= 1; }
@@ -238,20 +250,26 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
   __shared__ __align__(16) float s_ring[kRing][kRingPad + kTile];   // key masses, pooled in key order
   __shared__ __align__(16) float s_part[kRing][kSlices][kTile];     // per-slice sums of each key
   __shared__ WarpCompact s_wc;
+  __shared__ ListHand s_hand[2];
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = base;
+  const uint32_t sOnes = base;                       // the small blocks first: 12 KB, keeps sQ 1024-aligned
+  const uint32_t sBias = sOnes + kOnesBytes;
+  const uint32_t sQ = sBias + kBiasBytes;
   const uint32_t sK = sQ + (uint32_t)A.nq * 128 * NKH;
-  const uint32_t sOnes = sK + kStages2 * kTile * 128 * NKH;
-  const uint32_t sBias = sOnes + kTile * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     init_pipe_bars(&bars, kSmxWarps, kStages2);
     for (int i = 0; i < kRing; ++i) {
       tc::mbar_init(smem_u32(&rbars.rfull[i]), kSmxWarps);
-      tc::mbar_init(smem_u32(&rbars.rempty[i]), 1);
+      // a slot is free once its own pooling warp and the next tile's (which
+      // reads the last masses as its halo) are done with it
+      tc::mbar_init(smem_u32(&rbars.rempty[i]), 2);
+      tc::mbar_init(smem_u32(&rbars.mass[i]), 1);
     }
+    tc::mbar_init(smem_u32(&rbars.hand[0]), 1);
+    tc::mbar_init(smem_u32(&rbars.hand[1]), 1);
     tc::mbar_init(smem_u32(&rbars.bias_free), 1);
     s_abort = 0;
     tc::fence_barrier_init();
@@ -373,7 +391,13 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       }
     }
   } else {
-    // ------------------------------------------------------- pooling warp
+    // ------------------------------------------------------ pooling warps
+    // Warp `who` pools the tiles with tcount % 2 == who.  A tile's pad (the
+    // previous tile's last 2h masses) is read from the previous slot once
+    // its pooling warp has written them; the list state (count, threshold)
+    // comes from the previous tile's warp after its appends, so the list is
+    // written in key order.
+    const int who = warp - kPoolWarp;
     const float inv_pool = 1.0f / (float)A.pool_k;
     int tcount = 0;
     bool ok = true;
@@ -383,18 +407,17 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       const size_t slot_id = (size_t)blockIdx.x * A.maxseg + (size_t)(sg.bh - segs[0].bh);
       uint64_t* my_cand = CAND ? A.cand + slot_id * A.cap : nullptr;
       const int n_keep = CAND ? sel.n_sel[hk] : 0;
-      int cnt = 0;
-      long long tau = -1;
       const int n_iter = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
       for (int it = 0; it < n_iter; ++it, ++tcount) {
+        if ((tcount & 1) != who) continue;
         const int t0 = sg.a - hw + it * kTile;
         const int slot = tcount % kRing;
+        const int prev = (tcount + kRing - 1) % kRing;
         float* rr = s_ring[slot];   // [kRingPad - 2h, kRingPad): previous tile's last masses
-        if (it == 0) {
-          if (lane < kRingPad) rr[lane] = 0.f;   // keys before the segment's first tile: none
-          __syncwarp();
+        if (!wait_bar_warp(smem_u32(&rbars.rfull[slot]), (tcount / kRing) & 1, &s_abort, A.status, A.wait_limit)) {
+          ok = false;
+          break;
         }
-        if (!wait_bar_warp(smem_u32(&rbars.rfull[slot]), (tcount / kRing) & 1, &s_abort, A.status, A.wait_limit)) { ok = false; break; }
         {
           // key mass = the sum of its four slice sums; keys outside [0, S) weigh nothing
           const int jb = t0 + 4 * lane;
@@ -415,7 +438,21 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
           }
           *reinterpret_cast<float4*>(&rr[kRingPad + 4 * lane]) = m4;
           __syncwarp();
+          if (lane == 0) tc::mbar_arrive(smem_u32(&rbars.mass[slot]));
         }
+        // the pad: the previous tile's last 2h masses, or none at a segment start
+        if (it > 0) {
+          const int tp = tcount - 1;
+          if (!wait_bar_warp(smem_u32(&rbars.mass[prev]), (tp / kRing) & 1, &s_abort, A.status, A.wait_limit)) {
+            ok = false;
+            break;
+          }
+          if (lane < 2 * hw) rr[kRingPad - 2 * hw + lane] = s_ring[prev][kRingPad + kTile - 2 * hw + lane];
+        } else if (lane < kRingPad) {
+          rr[lane] = 0.f;
+        }
+        __syncwarp();
+        if (tcount > 0 && lane == 0) tc::mbar_arrive(smem_u32(&rbars.rempty[prev]));
         // lane l pools keys t0 - h + 4l + k, k = 0..3, over the masses of keys
         // t0 - 2h + 4l + k .. t0 + 4l + k, summed in ascending key order
         float sc[4];
@@ -463,6 +500,23 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
             const int jo = j0 + k;
             is_cand[k] = jo >= sg.a && jo < sg.b && jo >= sel.r_lo && jo < sel.r_hi;
           }
+          // the list as the previous tile of this segment left it (a new
+          // segment starts an empty list); the previous tile's hand-off is
+          // awaited even then, so its reader is done with the slot this
+          // tile's state overwrites
+          int cnt = 0;
+          long long tau = -1;
+          if (tcount > 0) {
+            const int tp = tcount - 1;
+            if (!wait_bar_warp(smem_u32(&rbars.hand[tp & 1]), (tp >> 1) & 1, &s_abort, A.status, A.wait_limit)) {
+              ok = false;
+              break;
+            }
+            if (it > 0) {
+              cnt = s_hand[tp & 1].cnt;
+              tau = s_hand[tp & 1].tau;
+            }
+          }
           // a key's place in the list: the candidates of lower lanes first,
           // then this lane's lower keys (four ballots, no scan)
           const unsigned lt = (1u << lane) - 1u;
@@ -493,14 +547,18 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
             cnt += n_new;
             break;
           }
+          if (lane == 0) {
+            s_hand[tcount & 1].cnt = cnt;
+            s_hand[tcount & 1].tau = tau;
+            if (it + 1 == n_iter) A.cand_cnt[slot_id] = cnt;
+          }
         }
-        // the next tile of this segment pools over this tile's last 2h masses
-        if (it + 1 < n_iter && lane < 2 * hw)
-          s_ring[(tcount + 1) % kRing][kRingPad - 2 * hw + lane] = rr[kRingPad + kTile - 2 * hw + lane];
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(smem_u32(&rbars.rempty[slot]));
+        if (lane == 0) {
+          tc::mbar_arrive(smem_u32(&rbars.hand[tcount & 1]));
+          tc::mbar_arrive(smem_u32(&rbars.rempty[slot]));
+        }
       }
-      if (CAND && ok && lane == 0) A.cand_cnt[slot_id] = cnt;
     }
   }
   tc::fence_before_sync();
@@ -587,8 +645,8 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
   CUtensorMap qm, km;
   if (!make_map(&qm, q, D, (uint64_t)B * H_q * W, 1, A.nq) || !make_map(&km, k, D, S, (uint64_t)B * H_kv, kTile))
     return cudaErrorInvalidValue;
-  const size_t smem = 1024 + (size_t)A.nq * 128 * (D / 64) + (size_t)kStages2 * kTile * 128 * (D / 64) +
-                      (size_t)kTile * 128 + (size_t)A.nq * 128;
+  const size_t smem = 1024 + kOnesBytes + kBiasBytes + (size_t)A.nq * 128 * (D / 64) +
+                      (size_t)kStages2 * kTile * 128 * (D / 64);
   const bool cand = out.cand != nullptr;
   if (D == 64)
     return cand ? launch(kvc_tc_pass2_kernel<64, true>, pl.P, smem, st, A, *sel, qm, km)
