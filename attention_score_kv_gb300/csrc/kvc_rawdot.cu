@@ -27,25 +27,50 @@ __device__ __forceinline__ int code8(float x, float inv) {
   return max(-127, min(127, c));
 }
 
-// One block per (b, KV head), one thread per dimension.
-__global__ void kvc_rawdot_query_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int W, int D,
-                                        int8_t* __restrict__ qcode, float* __restrict__ qscale) {
+// One block per (b, KV head).  The group's G*W contiguous window rows are
+// staged through shared memory in 32 KB chunks, 16-byte vectors with several
+// loads in flight per thread (a per-row global load chain would leave the
+// block waiting on one memory latency per row); then thread d < D sums
+// column d over the chunk's rows in (g, i) order.
+constexpr int kQueryThreads = 512;
+constexpr int kQueryChunkVecs = 2048;      // 32 KB of rows per chunk
+
+__global__ void __launch_bounds__(kQueryThreads)
+kvc_rawdot_query_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int W, int D,
+                        int8_t* __restrict__ qcode, float* __restrict__ qscale) {
+  __shared__ uint4 s_rows[kQueryChunkVecs];
+  __shared__ float s_max[kQueryThreads / 32];
   grid_dep_wait();
   grid_dep_launch();
   const int bh = blockIdx.x;
   const int b = bh / H_kv, h = bh % H_kv, G = H_q / H_kv;
   const int d = threadIdx.x;
-  const __nv_bfloat16* src = q + ((size_t)(b * H_q + h * G) * W) * D;
+  const int vec_per_row = D / 8;
+  const int chunk_rows = kQueryChunkVecs / vec_per_row;
+  const int rows = G * W;
+  const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)(b * H_q + h * G) * W) * D);
+  const __nv_bfloat16* srow = reinterpret_cast<const __nv_bfloat16*>(s_rows);
   float acc = 0.f;
-  for (int r = 0; r < G * W; ++r) acc = __fadd_rn(acc, __bfloat162float(src[(size_t)r * D + d]));
-  __shared__ float s_max[32];
-  float a = fabsf(acc);
+  for (int r0 = 0; r0 < rows; r0 += chunk_rows) {
+    const int nvec = min(chunk_rows, rows - r0) * vec_per_row;
+    const uint4* csrc = src + (size_t)r0 * vec_per_row;
+#pragma unroll 4
+    for (int v = threadIdx.x; v < nvec; v += kQueryThreads) s_rows[v] = __ldg(csrc + v);
+    __syncthreads();
+    if (d < D) {
+      const int nr = nvec / vec_per_row;
+      for (int r = 0; r < nr; ++r) acc = __fadd_rn(acc, __bfloat162float(srow[r * D + d]));
+    }
+    __syncthreads();
+  }
+  float a = d < D ? fabsf(acc) : 0.f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   if ((d & 31) == 0) s_max[d >> 5] = a;
   __syncthreads();
   float amax = 0.f;
   for (int w = 0; w < (D + 31) / 32; ++w) amax = fmaxf(amax, s_max[w]);
+  if (d >= D) return;
   const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
   qcode[(size_t)bh * D + d] = (int8_t)(amax > 0.f ? code8(acc, inv) : 0);
   if (d == 0) qscale[bh] = amax > 0.f ? __fdiv_rn(amax, 127.f) : 0.f;
@@ -122,6 +147,10 @@ kvc_rawdot_score_kernel(const __nv_bfloat16* __restrict__ k, int64_t rows, int64
   for (int t = 0; t < nchunks; ++t) {
     if (!scan::wait_bar_warp(smem_u32(&full[st]), ph, &s_abort, status)) break;
     const int64_t r0 = r_a + (int64_t)t * kRingRows;
+    // head of the stage's first row; a stage of kRingRows rows crosses at
+    // most one head boundary when S >= kRingRows
+    const int64_t h0 = r0 / S;
+    const int off0 = (int)(r0 - h0 * S);
 #pragma unroll
     for (int pass = 0; pass < kRingPasses; ++pass) {
       const int rr = (pass * kConsumerWarps + w) * RPW + sub;   // row within the stage
@@ -139,37 +168,43 @@ kvc_rawdot_score_kernel(const __nv_bfloat16* __restrict__ k, int64_t rows, int64
                        : "=r"(raw[i].x), "=r"(raw[i].y), "=r"(raw[i].z), "=r"(raw[i].w)
                        : "r"(rowaddr + chs[i] * 16));
       }
-      const int bh = (int)((valid ? r : r0) / S);
-      float a0 = 0.f, a1 = 0.f;
+      const int within = off0 + (valid ? rr : 0);
+      const int bh = (int)h0 + (S >= kRingRows ? (within >= S ? 1 : 0) : within / S);
+      // max |x| on bf16 pairs: exact, and the same value as in float32
+      __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
 #pragma unroll
       for (int i = 0; i < NLD; ++i) {
         const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(p2[e]);
-          a0 = fmaxf(a0, fabsf(f.x));
-          a1 = fmaxf(a1, fabsf(f.y));
-        }
+        for (int e = 0; e < 4; ++e) m2 = __hmax2(m2, __habs2(p2[e]));
       }
-      float a = fmaxf(a0, a1);
+      float a = fmaxf(__low2float(m2), __high2float(m2));
 #pragma unroll
       for (int o = LPR / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(group_mask, a, o));
-      // |x| <= a and inv = fl(127/a), so |x * inv| < 127.5: rint stays in
-      // [-127, 127] without a clamp
+      // |x| <= a and inv = fl(127/a), so y = fl(x * inv) has |y| < 127.5 and
+      // rint stays in [-127, 127] without a clamp.  rint(y) is taken by
+      // adding 1.5 * 2^23 in float32: the sum lies in [2^23, 2^24), where the
+      // spacing is 1, so round-to-nearest-even leaves y + 1.5 * 2^23 rounded
+      // to an integer with ties to even (1.5 * 2^23 is even), and the low
+      // byte of the sum's bit pattern is rint(y) mod 256, the code's
+      // two's-complement byte.
+      // The product and the sum are separate round-to-nearest intrinsics,
+      // which are never merged into a fused multiply-add.  (The packed
+      // f32x2 forms gave the codes of a single rounding on the GPU, so they
+      // are not used here.)
       const float inv = a > 0.f ? __fdiv_rn(127.f, a) : 0.f;
       int dot = 0;
 #pragma unroll
       for (int i = 0; i < NLD; ++i) {
-        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
-        int c[8];
+        const uint32_t* wd = reinterpret_cast<const uint32_t*>(&raw[i]);
+        uint32_t c[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(p2[e]);
-          c[2 * e] = __float2int_rn(__fmul_rn(f.x, inv));
-          c[2 * e + 1] = __float2int_rn(__fmul_rn(f.y, inv));
+          c[2 * e] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(wd[e] << 16), inv), 12582912.f));
+          c[2 * e + 1] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(wd[e] & 0xffff0000u), inv), 12582912.f));
         }
-        const int kp0 = (c[0] & 0xff) | ((c[1] & 0xff) << 8) | ((c[2] & 0xff) << 16) | (c[3] << 24);
-        const int kp1 = (c[4] & 0xff) | ((c[5] & 0xff) << 8) | ((c[6] & 0xff) << 16) | (c[7] << 24);
+        const int kp0 = (int)__byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+        const int kp1 = (int)__byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
         const int2 qp = *reinterpret_cast<const int2*>(qcode + (size_t)bh * D + chs[i] * 8);
         dot = __dp4a(kp0, qp.x, dot);
         dot = __dp4a(kp1, qp.y, dot);
@@ -192,7 +227,8 @@ kvc_rawdot_score_kernel(const __nv_bfloat16* __restrict__ k, int64_t rows, int64
 cudaError_t launch_rawdot_int8(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S,
                                int D, int W, int8_t* qcode, float* qscale, float* scores, cudaStream_t st) {
   const int BH = B * H_kv;
-  cudaError_t e = launch_pdl(kvc_rawdot_query_kernel, dim3(BH), dim3(D), 0, st, q, H_q, H_kv, W, D, qcode, qscale);
+  cudaError_t e = launch_pdl(kvc_rawdot_query_kernel, dim3(BH), dim3(kQueryThreads), 0, st, q, H_q, H_kv, W, D,
+                             qcode, qscale);
   note_launches(1);
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)BH * S;
