@@ -424,13 +424,10 @@ int kvc_score_rawdot_int8(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H
   if ((rc = check_ptr(q_win, 16, "q_win")) || (rc = check_ptr(k, 16, "k")) || (rc = check_ptr(scores, 4, "scores")))
     return rc;
   const size_t BH = (size_t)B * H_kv;
-  const size_t off_scale = align256(BH * (size_t)D);
-  if ((rc = check_ws(ws, ws_bytes, off_scale + BH * sizeof(float)))) return rc;
-  char* w = static_cast<char*>(ws);
+  if ((rc = check_ws(ws, ws_bytes, BH * (size_t)D * sizeof(float)))) return rc;
   return launch_status(launch_rawdot_int8(reinterpret_cast<const __nv_bfloat16*>(q_win),
                                           reinterpret_cast<const __nv_bfloat16*>(k), B, H_q, H_kv, S, D, W,
-                                          reinterpret_cast<int8_t*>(w), reinterpret_cast<float*>(w + off_scale),
-                                          scores, reinterpret_cast<cudaStream_t>(stream)),
+                                          static_cast<float*>(ws), scores, reinterpret_cast<cudaStream_t>(stream)),
                        "INT8 raw-product scorer launch");
 }
 

@@ -153,10 +153,10 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
                          const float* part_m, const float* part_z, float* bias_ws, int B, int H_q, int H_kv, int S,
                          int D, int W, int pool_k, const ScanPlan& pl, int gwp, const SelParams* sel, Pass2Out out,
                          bool inputs_ready, cudaStream_t st);
-// single-pass raw inner-product scores with INT8 keys: query codes and
-// scales of every head into qcode [BH][D] / qscale [BH], then dense scores
+// single-pass raw inner-product scores with INT8 keys: the scoring queries'
+// float32 column sums into qsum [BH][D], then dense scores
 cudaError_t launch_rawdot_int8(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H_q, int H_kv, int S,
-                               int D, int W, int8_t* qcode, float* qscale, float* scores, cudaStream_t st);
+                               int D, int W, float* qsum, float* scores, cudaStream_t st);
 // chunk j of the active layer's keys and values into its full-prompt buffer
 cudaError_t launch_append_chunk(const __nv_bfloat16* k_chunk, const __nv_bfloat16* v_chunk, int B, int H_kv, int S,
                                 int C, int D, int j, __nv_bfloat16* k_act, __nv_bfloat16* v_act, cudaStream_t st);

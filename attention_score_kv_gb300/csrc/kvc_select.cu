@@ -341,7 +341,9 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
 #pragma unroll
           for (int q = 0; q < kCopyBatch; ++q) {
             const int ff = f + q * kClThreads;
-            t[q] = ff < e ? __ldg(reinterpret_cast<const unsigned long long*>(src + ff)) : 0ull;
+            // written by the previous grid: a load through L2, not the
+            // read-only path
+            t[q] = ff < e ? __ldcg(reinterpret_cast<const unsigned long long*>(src + ff)) : 0ull;
           }
 #pragma unroll
           for (int q = 0; q < kCopyBatch; ++q) {

@@ -138,8 +138,9 @@ int kvc_score_pass2_pool(const kvc_bf16* q_win, const kvc_bf16* k,
  *          scoring query, each key) is cast to symmetric INT8 with
  *          code = rint(x * (127 / max|x|)) in [-127, 127], scale = max|x| /
  *          127, and dot_j is the exact integer product of the codes.
- *   ws     >= B*H_kv*(D + 4) + 256 bytes, 256-byte aligned (the query codes
- *          and scales); kvc_workspace_size(...) bytes always suffice.
+ *   ws     >= B*H_kv*D*4 bytes, 256-byte aligned (the scoring queries'
+ *          float32 column sums); kvc_workspace_size(...) bytes always
+ *          suffice.
  * Rank the scores with kvc_select_topk and fetch the full-precision rows
  * with kvc_gather.  Errors as for the other calls.
  */
