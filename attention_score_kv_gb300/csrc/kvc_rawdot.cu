@@ -52,8 +52,17 @@ kvc_rawdot_qsum_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, i
     if (c < nr) s_rows[c] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(r0 + c) * D));
     __syncthreads();
     if (c < 8) {
+      // 16 loads in flight, then the ordered adds
       const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(s_rows);
-      for (int r = 0; r < nr; ++r) acc = __fadd_rn(acc, __bfloat162float(sv[r * 8 + c]));
+      int r = 0;
+      for (; r + 16 <= nr; r += 16) {
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v[u] = __bfloat162float(sv[(r + u) * 8 + c]);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) acc = __fadd_rn(acc, v[u]);
+      }
+      for (; r < nr; ++r) acc = __fadd_rn(acc, __bfloat162float(sv[r * 8 + c]));
     }
     __syncthreads();
   }
