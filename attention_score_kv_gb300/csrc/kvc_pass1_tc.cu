@@ -64,6 +64,20 @@ __device__ __forceinline__ float2 batch_sum(const float* v, float c2, float nm) 
   return __fadd2_rn(__fadd2_rn(a0, a1), __fadd2_rn(a2, a3));
 }
 
+// A batch whose sum would pass 2^60 (a score far above the reference),
+// redone against a raised reference.  Rare, and out of line so that the
+// unrolled hot loop stays short: the values come in a local copy, and the
+// arithmetic is the hot path's, in the same order.
+template <int N>
+__device__ __noinline__ float2 redo_batch(const float* v, float c2, float2 z2, float* mref) {
+  const float mnew = fmaxf(*mref, batch_max<N>(v));
+  const float sc = ex2((*mref - mnew) * c2);
+  z2.x *= sc;
+  z2.y *= sc;
+  *mref = mnew;
+  return __fadd2_rn(z2, batch_sum<N>(v, c2, -mnew * c2));
+}
+
 // MMA issuer `who` (0 or 1) of pass 1: sub-tiles u = NMB * tile + block with
 // u % 2 == who, in order.  A tile's ring stage is released by a commit of
 // each issuer that used it; the queries of a segment, by a commit of both.
@@ -225,16 +239,15 @@ kvc_tc_pass1_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         // the same log-sum-exp.
         if (mref == -INFINITY) mref = batch_max<NCW>(v);
         if (mref > -INFINITY) {
-          float2 bs = batch_sum<NCW>(v, c2, -mref * c2);
+          const float2 bs = batch_sum<NCW>(v, c2, -mref * c2);
           if (!(bs.x + bs.y <= kBatchSumLimit)) {
-            const float mnew = fmaxf(mref, batch_max<NCW>(v));
-            const float sc = ex2((mref - mnew) * c2);
-            z2.x *= sc;
-            z2.y *= sc;
-            mref = mnew;
-            bs = batch_sum<NCW>(v, c2, -mref * c2);
+            float vv[NCW];
+#pragma unroll
+            for (int c = 0; c < NCW; ++c) vv[c] = v[c];
+            z2 = redo_batch<NCW>(vv, c2, z2, &mref);
+          } else {
+            z2 = __fadd2_rn(z2, bs);
           }
-          z2 = __fadd2_rn(z2, bs);
         }
       }
       // segment done: the NPART column slices of a row are merged in slice order

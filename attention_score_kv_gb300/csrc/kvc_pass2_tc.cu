@@ -71,8 +71,10 @@ __device__ __forceinline__ uint32_t bf16_bits(float x) {
 
 // One warp keeps the n_keep best entries of buf[0..cnt) in place (order
 // kept) by an 8-bit radix select on rank_key, and returns the new count;
-// *tau becomes the score bits a later (higher-index) key must beat.
-__device__ int warp_compact(uint64_t* buf, int cnt, int n_keep, WarpCompact* wc, long long* tau, int* status) {
+// *tau becomes the score bits a later (higher-index) key must beat.  Out of
+// line: it runs only when a list fills, and the pooling warps' hot code
+// stays short (the pass ran about 1 us faster per layer).
+__device__ __noinline__ int warp_compact(uint64_t* buf, int cnt, int n_keep, WarpCompact* wc, long long* tau, int* status) {
   const int lane = threadIdx.x & 31;
   if (n_keep <= 0) {
     *tau = LLONG_MAX;
@@ -235,6 +237,21 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
     }
     if (!__shfl_sync(0xffffffffu, okl, 0)) return;
   }
+}
+
+// The pooled scores of four keys for a pool width other than 7 (the
+// long-context workloads use 7), out of line: the window's masses summed
+// in ascending key order, as the inline 7-wide path does.
+__device__ __noinline__ float4 pool_generic(const float* rr, int hw, int pool_k, float inv_pool) {
+  const int lane = threadIdx.x & 31;
+  const float* win = rr + kRingPad - 2 * hw + 4 * lane;
+  float sc[4];
+  for (int k = 0; k < 4; ++k) {
+    float acc = 0.f;
+    for (int d = 0; d <= 2 * hw; ++d) acc += win[k + d];
+    sc[k] = pool_k == 1 ? acc : acc * inv_pool;
+  }
+  return make_float4(sc[0], sc[1], sc[2], sc[3]);
 }
 
 template <int D, bool CAND>
@@ -472,18 +489,11 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
             sc[k] = acc * inv_pool;
           }
         } else {
-          const float* win = rr + kRingPad - 2 * hw + 4 * lane;
-          float wv[4 + kRingPad];
-#pragma unroll
-          for (int i = 0; i < 4 + kRingPad; ++i) wv[i] = (i < 4 + 2 * hw) ? win[i] : 0.f;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float acc = 0.f;
-#pragma unroll
-            for (int d = 0; d <= kRingPad; ++d)
-              if (d <= 2 * hw) acc += wv[k + d];
-            sc[k] = A.pool_k == 1 ? acc : acc * inv_pool;
-          }
+          const float4 g4 = pool_generic(rr, hw, A.pool_k, inv_pool);
+          sc[0] = g4.x;
+          sc[1] = g4.y;
+          sc[2] = g4.z;
+          sc[3] = g4.w;
         }
         const int j0 = t0 - hw + 4 * lane;
         if (!CAND) {
