@@ -59,6 +59,7 @@ struct ListHand {
 struct WarpCompact {
   int hist[256];
 };
+constexpr int kCompactBatch = 4;   // list entries per lane in flight while compacting
 
 __device__ __forceinline__ uint64_t rank_key(uint64_t e) {
   // (score bits, ~index): larger is better, the lower index wins a score tie
@@ -85,9 +86,20 @@ __device__ __noinline__ int warp_compact(uint64_t* buf, int cnt, int n_keep, War
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) wc->hist[i] = 0;
     __syncwarp();
-    for (int i = lane; i < cnt; i += 32) {
-      const uint64_t key = rank_key(buf[i]);
-      if (shift == 56 || (key >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&wc->hist[(key >> shift) & 255], 1);
+    // kCompactBatch independent loads in flight per lane
+    for (int i0 = 0; i0 < cnt; i0 += 32 * kCompactBatch) {
+      uint64_t e[kCompactBatch];
+#pragma unroll
+      for (int q = 0; q < kCompactBatch; ++q) {
+        const int i = i0 + 32 * q + lane;
+        e[q] = i < cnt ? buf[i] : 0ull;
+      }
+#pragma unroll
+      for (int q = 0; q < kCompactBatch; ++q) {
+        const uint64_t key = rank_key(e[q]);
+        if (i0 + 32 * q + lane < cnt && (shift == 56 || (key >> (shift + 8)) == (prefix >> (shift + 8))))
+          atomicAdd(&wc->hist[(key >> shift) & 255], 1);
+      }
     }
     __syncwarp();
     int local = 0;
@@ -131,14 +143,23 @@ __device__ __noinline__ int warp_compact(uint64_t* buf, int cnt, int n_keep, War
   }
   const uint64_t T = prefix;
   int out = 0;
-  for (int b0 = 0; b0 < cnt; b0 += 32) {
-    const int i = b0 + lane;
-    const uint64_t e = i < cnt ? buf[i] : 0ull;
-    const bool f = i < cnt && rank_key(e) >= T;
-    const unsigned bal = __ballot_sync(0xffffffffu, f);
-    __syncwarp();
-    if (f) buf[out + __popc(bal & ((1u << lane) - 1u))] = e;
-    out += __popc(bal);
+  // In place: a batch reads all of [b0, b0 + 32 * kCompactBatch) before it
+  // writes, and every write lands below b0 + 32 * kCompactBatch (out never
+  // passes the entries read), so no entry is overwritten before it is read.
+  for (int b0 = 0; b0 < cnt; b0 += 32 * kCompactBatch) {
+    uint64_t e[kCompactBatch];
+#pragma unroll
+    for (int q = 0; q < kCompactBatch; ++q) {
+      const int i = b0 + 32 * q + lane;
+      e[q] = i < cnt ? buf[i] : 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < kCompactBatch; ++q) {
+      const bool f = b0 + 32 * q + lane < cnt && rank_key(e[q]) >= T;
+      const unsigned bal = __ballot_sync(0xffffffffu, f);
+      if (f) buf[out + __popc(bal & ((1u << lane) - 1u))] = e[q];
+      out += __popc(bal);
+    }
     __syncwarp();
   }
   if (out != n_keep && lane == 0) record_status(status, kStatusCandOverflow);
