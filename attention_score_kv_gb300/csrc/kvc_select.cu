@@ -57,7 +57,7 @@ __device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int p
 // only the keys that share its digit (when they fit), so the later rounds
 // histogram those alone.
 constexpr int kMaxCl = 16;              // CTAs per head at most (a non-portable cluster size)
-constexpr int kClThreads = 512;
+constexpr int kClThreads = 1024;
 constexpr int kClWarps = kClThreads / 32;
 constexpr int kStageC = 16384;          // entries per CTA kept in shared memory (clusters of <= 8)
 constexpr int kStageC16 = 8192;         // ... in clusters of 16, two CTAs per SM
@@ -266,7 +266,7 @@ __device__ void cl_resolve(ClSmem* cs, int round, int need, int* digit, int* nee
 }
 
 template <int kCl>
-__global__ void __launch_bounds__(kClThreads, kCl == 16 ? 2 : 1)
+__global__ void __launch_bounds__(kClThreads, 1)
 kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap, int32_t* __restrict__ idx,
                   int* status) {
   extern __shared__ __align__(16) uint8_t cl_dyn[];
