@@ -379,20 +379,14 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(smem_u32(&bars.tempty[buf]));
-        // Columns that carry no weight become -inf (2^-inf = 0): chunks
-        // past this warp's slice, and, in tiles near the window, the window
+        // Chunks past this warp's slice carry no weight and are skipped (a
+        // warp-uniform test per chunk: G*W = 128 fills only half of the 16
+        // chunks, G*W = 160 ten); in tiles near the window, the window
         // queries a key comes after (query i of column g*W + i sees key j
-        // only when j <= S - W + i).  Every key then runs the same
-        // arithmetic in the same order, so keys with equal inputs get
-        // bit-identical masses wherever they sit.
-        if (c0 + 4 > c_end) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (c0 + i >= c_end) {
-#pragma unroll
-              for (int q = 0; q < 16; ++q) v[16 * i + q] = -INFINITY;
-            }
-        }
+        // only when j <= S - W + i) become -inf (2^-inf = 0).  Every key
+        // then runs the same arithmetic in the same order, so keys with equal
+        // inputs get bit-identical masses wherever they sit.
+        const int nv = c_end - c0;   // chunks of this warp that carry weight
         if (t0 + kTile - 1 > A.S - A.W) {
           const int dj = t0 + krow - (A.S - A.W);
           if (dj > 0) {
@@ -406,15 +400,20 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         }
         float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-          const float2 x0 = __fmul2_rn(make_float2(v[c], v[c + 1]), cc);
-          const float2 x1 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), cc);
-          const float2 x2 = __fmul2_rn(make_float2(v[c + 4], v[c + 5]), cc);
-          const float2 x3 = __fmul2_rn(make_float2(v[c + 6], v[c + 7]), cc);
-          a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
-          a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
-          a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
-          a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+        for (int ch = 0; ch < 4; ++ch) {
+          if (ch < nv) {
+#pragma unroll
+            for (int c = 16 * ch; c < 16 * ch + 16; c += 8) {
+              const float2 x0 = __fmul2_rn(make_float2(v[c], v[c + 1]), cc);
+              const float2 x1 = __fmul2_rn(make_float2(v[c + 2], v[c + 3]), cc);
+              const float2 x2 = __fmul2_rn(make_float2(v[c + 4], v[c + 5]), cc);
+              const float2 x3 = __fmul2_rn(make_float2(v[c + 6], v[c + 7]), cc);
+              a0 = __fadd2_rn(a0, make_float2(ex2(x0.x), ex2(x0.y)));
+              a1 = __fadd2_rn(a1, make_float2(ex2(x1.x), ex2(x1.y)));
+              a2 = __fadd2_rn(a2, make_float2(ex2(x2.x), ex2(x2.y)));
+              a3 = __fadd2_rn(a3, make_float2(ex2(x3.x), ex2(x3.y)));
+            }
+          }
         }
         const float r = (a0.x + a0.y) + (a1.x + a1.y) + ((a2.x + a2.y) + (a3.x + a3.y));
         const int slot = tcount % kRing;
