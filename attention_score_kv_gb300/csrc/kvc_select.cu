@@ -528,9 +528,10 @@ cudaError_t launch_select(int mode, const float* scores, const uint64_t* cand, c
   };
   if (smem_for(kStageC) > 200 * 1024) return cudaErrorInvalidConfiguration;
   // the widest cluster that still gives every head its own CTAs in one wave;
-  // 16 (two CTAs per SM, smaller shared-memory shares) only where the device
-  // co-schedules a cluster of 16 for every head at once
-  // (short heads keep clusters of 8: their shares are small already)
+  // 16 (smaller shared-memory shares) only where the device co-schedules a
+  // cluster of 16 for every head at once.  Short heads keep clusters of 8:
+  // narrower clusters were slower there (Llama 8K: 18.6 us at 8, 21.6 at 2,
+  // 24.8 at 1), the cluster's parallel sweeps outweigh its barriers.
   int cl = sel.S >= 65536 ? kMaxCl : 8;
   while (cl > 1 && (int64_t)BH * cl > num_sms()) cl >>= 1;
   auto pick = [](int c) {
