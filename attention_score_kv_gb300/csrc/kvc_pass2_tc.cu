@@ -570,9 +570,21 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
               continue;
             }
             int pos = cnt + before;
+            if (take[0] && take[1] && take[2] && take[3] && ((reinterpret_cast<uintptr_t>(my_cand + pos) & 15u) == 0)) {
+              // all four keys of the lane (the common case while the list has
+              // room): two 16-byte stores, so a warp writes 1 KB contiguously
+              ulonglong2 e01, e23;
+              e01.x = ((uint64_t)u[0] << 32) | (uint32_t)(j0 + 0);
+              e01.y = ((uint64_t)u[1] << 32) | (uint32_t)(j0 + 1);
+              e23.x = ((uint64_t)u[2] << 32) | (uint32_t)(j0 + 2);
+              e23.y = ((uint64_t)u[3] << 32) | (uint32_t)(j0 + 3);
+              *reinterpret_cast<ulonglong2*>(my_cand + pos) = e01;
+              *reinterpret_cast<ulonglong2*>(my_cand + pos + 2) = e23;
+            } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              if (take[k]) my_cand[pos++] = ((uint64_t)u[k] << 32) | (uint32_t)(j0 + k);
+              for (int k = 0; k < 4; ++k) {
+                if (take[k]) my_cand[pos++] = ((uint64_t)u[k] << 32) | (uint32_t)(j0 + k);
+              }
             }
             cnt += n_new;
             break;
