@@ -192,6 +192,20 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
   for (int i = lane; i < A.nq * 2; i += 32)
     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(sBias + i * 16), "r"(0u) : "memory");
   uint32_t stage = 0, phase = 0, qphase = 0, buf = 0, tphase = 0, bphase = 0;
+  // query side of the bias K-step: row q, K elements 0..2 = the row's bias
+  // split into three bf16 terms; lane l handles rows l, l+32, ....  The
+  // next segment's biases are loaded as soon as the current segment's
+  // operand is written, so they are in registers by the time its MMAs drain
+  // (fetched at the switch, they held the switch up by about 3 us).
+  float bv[kMaxGWP / 32];
+  auto load_bias = [&](int si) {
+#pragma unroll
+    for (int i = 0; i < kMaxGWP / 32; ++i) {
+      const int row = lane + 32 * i;
+      bv[i] = (row < A.gwp16) ? A.bias[(size_t)segs[si].bh * A.gwp16 + row] : kNoWeight;
+    }
+  };
+  load_bias(0);
   for (int s = 0; s < nseg; ++s) {
     const Seg sg = segs[s];
     int okl = 1;
@@ -200,14 +214,6 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
       bphase ^= 1;
     }
     if (!__shfl_sync(0xffffffffu, okl, 0)) return;
-    // query side: row q, K elements 0..2 = bias split into three bf16 terms;
-    // lane l handles rows l, l+32, ...: all loads first, then the stores
-    float bv[kMaxGWP / 32];
-#pragma unroll
-    for (int i = 0; i < kMaxGWP / 32; ++i) {
-      const int row = lane + 32 * i;
-      bv[i] = (row < A.gwp16) ? A.bias[(size_t)sg.bh * A.gwp16 + row] : kNoWeight;
-    }
 #pragma unroll
     for (int i = 0; i < kMaxGWP / 32; ++i) {
       const int row = lane + 32 * i;
@@ -226,6 +232,7 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
     }
     tc::fence_proxy_async();
     __syncwarp();
+    if (s + 1 < nseg) load_bias(s + 1);
     if (lane == 0) {
       if (!wait_bar(smem_u32(&bars->qfull), qphase, abort_flag, A.status, A.wait_limit)) okl = 0;
       qphase ^= 1;
