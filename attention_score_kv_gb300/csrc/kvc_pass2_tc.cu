@@ -169,7 +169,7 @@ __device__ __noinline__ int warp_compact(uint64_t* buf, int cnt, int n_keep, War
 
 // Whole warp: writes the bias operand of each segment (after the previous
 // segment's MMAs are done with it); lane 0 issues the MMAs.
-template <int D>
+template <int D, int NL>
 __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const Seg* segs, int nseg, uint32_t sQ,
                          uint32_t sK, uint32_t sOnes, uint32_t sBias, uint32_t tmem, volatile int* abort_flag) {
   constexpr int NKH = D / 64;
@@ -245,7 +245,7 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
         }
         tc::fence_after_sync();
         const uint32_t kb = sK + stage * kTileBytes;
-        const uint32_t dacc = tmem + buf * kAccStride;
+        const uint32_t dacc = tmem + buf * (NL == 4 ? 256u : 128u);
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
           const uint32_t koff = (ks >> 2) * (kTile * 128) + (ks & 3) * 32;
@@ -256,7 +256,7 @@ __device__ void mma_warp(const ScanArgs& A, PipeBars* bars, RingBars* rb, const 
         tc::mma_commit(smem_u32(&bars->empty[stage]));
         tc::mma_commit(smem_u32(&bars->tfull[buf]));
         if (++stage == kStages2) { stage = 0; phase ^= 1; }
-        if (++buf == 2) { buf = 0; tphase ^= 1; }
+        if (++buf == (NL == 4 ? 2u : 4u)) { buf = 0; tphase ^= 1; }
       }
       if (okl) {
         tc::mma_commit(smem_u32(&bars->qempty));
@@ -282,7 +282,12 @@ __device__ __noinline__ float4 pool_generic(const float* rr, int hw, int pool_k,
   return make_float4(sc[0], sc[1], sc[2], sc[3]);
 }
 
-template <int D, bool CAND>
+// NL: 16-column accumulator chunks each softmax warp loads.  Windows of up
+// to 128 rows (G*W <= 128: at most two chunks a warp) run with NL = 2 and
+// four 128-column accumulators in tensor memory, so the MMA runs up to four
+// tiles ahead of the exponentials; wider windows with NL = 4 and two
+// 256-column accumulators.
+template <int D, bool CAND, int NL>
 __global__ void __launch_bounds__(kThreads, 1)
 kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ SelParams sel,
                     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap) {
@@ -344,14 +349,16 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       producer<D, 2, kStages2>(A, &qmap, &kmap, &bars, sQ, sK, &s_abort);
     }
   } else if (warp == 1) {
-    mma_warp<D>(A, &bars, &rbars, segs, nseg, sQ, sK, sOnes, sBias, tmem, &s_abort);
+    mma_warp<D, NL>(A, &bars, &rbars, segs, nseg, sQ, sK, sOnes, sBias, tmem, &s_abort);
     if (lane == 0) drain_mma(smem_u32(&bars.drain[0]), A.status);   // its MMAs are done before TMEM is freed
   } else if (warp < kPoolWarp) {
     // ---------------------------------------------------- softmax warps
     // Warp k of a lane quarter owns column chunks [k*cw, k*cw + cw) of the
-    // G*W (rounded to 16) window columns, cw = ceil(chunks / 4) <= 4.  It
-    // always loads four 16-column chunks (they stay inside the 256-column
-    // buffer); chunks past its slice or past the last one weigh nothing.
+    // G*W (rounded to 16) window columns, cw = ceil(chunks / 4) <= NL.  It
+    // always loads NL 16-column chunks (they stay inside its accumulator:
+    // columns c0*16 .. c0*16 + 16*NL - 1 with c0 <= 3*cw, at most 127 of 128
+    // with NL = 2 and 255 of 256 with NL = 4); chunks past its slice or past
+    // the last one weigh nothing.
     const int k = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int krow = quarter * 32 + lane;
@@ -369,19 +376,20 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
       const int n_iter = (sg.b - sg.a + 2 * hw + kTile - 1) / kTile;
       for (int it = 0; it < n_iter; ++it, ++tcount) {
         const int t0 = sg.a - hw + it * kTile;
-        const uint32_t buf = (uint32_t)tcount & 1u;
-        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), ((uint32_t)tcount >> 1) & 1u, &s_abort, A.status,
+        constexpr uint32_t kBufs = NL == 4 ? 2u : 4u, kCols = NL == 4 ? 256u : 128u;
+        const uint32_t buf = (uint32_t)tcount % kBufs;
+        if (!wait_bar_warp(smem_u32(&bars.tfull[buf]), ((uint32_t)tcount / kBufs) & 1u, &s_abort, A.status,
                            A.wait_limit)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        float v[64];
-        const uint32_t taddr = tmem + buf * kAccStride + tlane + (uint32_t)c0 * 16;
+        float v[16 * NL];
+        const uint32_t taddr = tmem + buf * kCols + tlane + (uint32_t)c0 * 16;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tc::tmem_ld16(taddr + i * 16, v + 16 * i);
+        for (int i = 0; i < NL; ++i) tc::tmem_ld16(taddr + i * 16, v + 16 * i);
         tc::tmem_wait_ld();
-        tc::reg_fence(v, 64);
+        tc::reg_fence(v, 16 * NL);
         // the accumulator is free for the MMA warp as soon as it is in registers
         tc::fence_before_sync();
         __syncwarp();
@@ -399,7 +407,7 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
           if (dj > 0) {
             int wi = (c0 * 16) % A.W;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+            for (int c = 0; c < 16 * NL; ++c) {
               if (wi < dj) v[c] = -INFINITY;
               if (++wi == A.W) wi = 0;
             }
@@ -407,7 +415,7 @@ kvc_tc_pass2_kernel(const __grid_constant__ ScanArgs A, const __grid_constant__ 
         }
         float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < NL; ++ch) {
           if (ch < nv) {
 #pragma unroll
             for (int c = 16 * ch; c < 16 * ch + 16; c += 8) {
@@ -697,11 +705,19 @@ cudaError_t launch_pass2(const __nv_bfloat16* q, const __nv_bfloat16* k, const f
   const size_t smem = 1024 + kOnesBytes + kBiasBytes + (size_t)A.nq * 128 * (D / 64) +
                       (size_t)kStages2 * kTile * 128 * (D / 64);
   const bool cand = out.cand != nullptr;
-  if (D == 64)
-    return cand ? launch(kvc_tc_pass2_kernel<64, true>, pl.P, smem, st, A, *sel, qm, km)
-                : launch(kvc_tc_pass2_kernel<64, false>, pl.P, smem, st, A, *sel, qm, km);
-  return cand ? launch(kvc_tc_pass2_kernel<128, true>, pl.P, smem, st, A, *sel, qm, km)
-              : launch(kvc_tc_pass2_kernel<128, false>, pl.P, smem, st, A, *sel, qm, km);
+  const bool narrow = A.gwp16 <= 128;   // two chunks a softmax warp, four accumulators
+  if (D == 64) {
+    if (narrow)
+      return cand ? launch(kvc_tc_pass2_kernel<64, true, 2>, pl.P, smem, st, A, *sel, qm, km)
+                  : launch(kvc_tc_pass2_kernel<64, false, 2>, pl.P, smem, st, A, *sel, qm, km);
+    return cand ? launch(kvc_tc_pass2_kernel<64, true, 4>, pl.P, smem, st, A, *sel, qm, km)
+                : launch(kvc_tc_pass2_kernel<64, false, 4>, pl.P, smem, st, A, *sel, qm, km);
+  }
+  if (narrow)
+    return cand ? launch(kvc_tc_pass2_kernel<128, true, 2>, pl.P, smem, st, A, *sel, qm, km)
+                : launch(kvc_tc_pass2_kernel<128, false, 2>, pl.P, smem, st, A, *sel, qm, km);
+  return cand ? launch(kvc_tc_pass2_kernel<128, true, 4>, pl.P, smem, st, A, *sel, qm, km)
+              : launch(kvc_tc_pass2_kernel<128, false, 4>, pl.P, smem, st, A, *sel, qm, km);
 }
 
 }  // namespace kvc
