@@ -311,6 +311,9 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
   const int f0 = (int)((int64_t)E * rank / kCl), f1 = (int)((int64_t)E * (rank + 1) / kCl);
   const int n = f1 - f0;
   const int mode = n_sel <= 0 ? 0 : n_sel >= E ? 2 : 1;
+  // when the whole share fits in shared memory, the first radix round's
+  // histogram is taken as the entries arrive, not in a pass of its own
+  const bool hist0_in_copy = mode == 1 && n <= stage_cap;
 
   // copy this CTA's share into shared memory, list by list
   if (mode != 0) {
@@ -326,7 +329,10 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
 #pragma unroll
         for (int q = 0; q < kCopyBatch; ++q) {
           const int i = i0 + q * kClThreads + threadIdx.x;
-          if (i < ns) stage[i] = t[q];
+          if (i < ns) {
+            stage[i] = t[q];
+            if (hist0_in_copy) atomicAdd(&cs.hist[(uint32_t)(t[q] >> 53)], 1u);
+          }
         }
       }
     } else {
@@ -348,7 +354,10 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
 #pragma unroll
           for (int q = 0; q < kCopyBatch; ++q) {
             const int ff = f + q * kClThreads;
-            if (ff < e) stage[ff - f0] = t[q];
+            if (ff < e) {
+              stage[ff - f0] = t[q];
+              if (hist0_in_copy) atomicAdd(&cs.hist[(uint32_t)(t[q] >> 53)], 1u);
+            }
           }
         }
       }
@@ -368,7 +377,7 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
       if (round == 1) ns = cl_survivors(hv, stage, f0, n, prefix, &cs, cs.hist, kHist1);
       if (round > 0 && ns >= 0)
         cl_hist_surv(cs.hist, ns, round, prefix, hr);
-      else
+      else if (round > 0 || !hist0_in_copy)
         cl_hist(hv, stage, f0, n, round, prefix, hr);
       cluster_sync_all();
       int d, nd;
