@@ -97,7 +97,7 @@ struct __align__(16) ClSmem {
   int scan[32];
   int digit, need;
   int wgt[kClWarps], weq[kClWarps], wout[kClWarps], weqb[kClWarps];
-  int wsurv[kClWarps], nsurv;                // keys that share the round-0 digit: per warp, in total
+  int nsurv, surv_fill;                      // keys that share the round-0 digit; survivors placed
   int cta_gt, cta_eq;                        // this CTA's keys above / at the threshold
 };
 
@@ -163,43 +163,32 @@ __device__ void cl_hist_surv(const uint32_t* surv, int ns, int round, uint32_t p
 }
 
 // After round 0: the score bits of this CTA's keys whose top 11 bits equal
-// d0 are copied, in key order, into surv (the round-0 histogram, which no
-// CTA reads any more), when they fit; returns their number, or -1 when they
-// do not fit and the later rounds scan the whole share.
+// d0 are copied, in no particular order, into surv (the round-0 histogram,
+// which no CTA reads any more), when they fit; returns their number (this
+// CTA's round-0 count of d0), or -1 when they do not fit and the later rounds
+// scan the whole share.  Each warp claims room for its survivors with one
+// shared-memory atomic per 32 entries.
 __device__ int cl_survivors(const HeadView& hv, const uint64_t* stage, int f0, int n, uint32_t d0, ClSmem* cs,
                             uint32_t* surv, int cap) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int chunk = (n + kClWarps - 1) / kClWarps;
-  const int lo = min(n, w * chunk), hi = min(n, lo + chunk);
-  int cnt = 0;
-  for (int i0 = lo; i0 < hi; i0 += 32) {
-    const int i = i0 + lane;
-    const bool keep = i < hi && (uint32_t)(share_entry(hv, stage, f0, n, i) >> 53) == d0;
-    cnt += __popc(__ballot_sync(0xffffffffu, keep));
-  }
-  if (lane == 0) cs->wsurv[w] = cnt;
-  __syncthreads();
   if (threadIdx.x == 0) {
-    int t = 0;
-    for (int q = 0; q < kClWarps; ++q) {
-      const int c = cs->wsurv[q];
-      cs->wsurv[q] = t;
-      t += c;
-    }
-    cs->nsurv = t;
+    cs->nsurv = (int)surv[d0];
+    cs->surv_fill = 0;
   }
   __syncthreads();
   const int total = cs->nsurv;
   if (total > cap) return -1;
-  int pos = cs->wsurv[w];
+  const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
-  for (int i0 = lo; i0 < hi; i0 += 32) {
-    const int i = i0 + lane;
-    const uint32_t u = i < hi ? (uint32_t)(share_entry(hv, stage, f0, n, i) >> 32) : 0u;
-    const bool keep = i < hi && (u >> 21) == d0;
+  for (int i0 = 0; i0 < n; i0 += kClThreads) {
+    const int i = i0 + threadIdx.x;
+    const uint32_t u = i < n ? (uint32_t)(share_entry(hv, stage, f0, n, i) >> 32) : 0u;
+    const bool keep = i < n && (u >> 21) == d0;
     const unsigned b = __ballot_sync(0xffffffffu, keep);
-    if (keep) surv[pos + __popc(b & lt)] = u;
-    pos += __popc(b);
+    int base = 0;
+    if (lane == 0 && b != 0u) base = atomicAdd(&cs->surv_fill, __popc(b));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int at = base + __popc(b & lt);
+    if (keep && at < cap) surv[at] = u;
   }
   __syncthreads();
   return total;
