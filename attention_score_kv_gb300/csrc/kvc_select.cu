@@ -59,6 +59,7 @@ __device__ __forceinline__ int64_t cand_slot(const SelParams& sp, int seg, int p
 constexpr int kMaxCl = 16;              // CTAs per head at most (a non-portable cluster size)
 constexpr int kClThreads = 1024;
 constexpr int kClWarps = kClThreads / 32;
+static_assert(kClWarps <= 32, "one warp holds the per-warp counts");
 constexpr int kStageC = 16384;          // entries per CTA kept in shared memory (clusters of <= 8)
 constexpr int kStageC16 = 8192;         // ... in clusters of 16, two CTAs per SM
 constexpr int kCopyBatch = 8;
@@ -399,11 +400,17 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
   }
   if (lane == 0) { cs.wgt[w] = gtw; cs.weq[w] = eqw; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int g = 0, e = 0;
-    for (int q = 0; q < kClWarps; ++q) { g += cs.wgt[q]; e += cs.weq[q]; }
-    cs.cta_gt = g;
-    cs.cta_eq = e;
+  if (w == 0) {   // lane q holds warp q's counts
+    int g = lane < kClWarps ? cs.wgt[lane] : 0, e = lane < kClWarps ? cs.weq[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if (lane == 0) {
+      cs.cta_gt = g;
+      cs.cta_eq = e;
+    }
   }
   cluster_sync_all();
 
@@ -429,14 +436,26 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) took += __shfl_xor_sync(0xffffffffu, took, o);
     const int eb_all = __shfl_sync(0xffffffffu, e_incl, 31);
-    if (threadIdx.x == 0) {
-      int ob = took, eb = eb_all;
-      for (int q = 0; q < kClWarps; ++q) {
-        cs.wout[q] = ob;
-        cs.weqb[q] = eb;
-        ob += cs.wgt[q] + (mode == 2 ? 0 : max(0, min(cs.weq[q], need_eq - eb)));
-        eb += cs.weq[q];
-      }
+    // lane q: where warp q's stretch starts writing (after the lower CTAs'
+    // keys and the keys warps 0 .. q-1 take) and how many ties come before it
+    const int qg = r < kClWarps ? cs.wgt[r] : 0, qe = r < kClWarps ? cs.weq[r] : 0;
+    int qe_incl = qe;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, qe_incl, o);
+      if (r >= o) qe_incl += t;
+    }
+    const int eb = eb_all + qe_incl - qe;
+    const int qtake = qg + (mode == 2 ? 0 : max(0, min(qe, need_eq - eb)));
+    int qt_incl = qtake;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, qt_incl, o);
+      if (r >= o) qt_incl += t;
+    }
+    if (r < kClWarps) {
+      cs.wout[r] = took + qt_incl - qtake;
+      cs.weqb[r] = eb;
     }
   }
   __syncthreads();
