@@ -67,6 +67,12 @@ constexpr int kCopyBatch = 8;
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
@@ -271,6 +277,10 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
   const int nparts = v.mode == 0 ? 1 : sp.nparts;
 
   for (int i = threadIdx.x; i < kHist1 + kHist2 + kHist3; i += kClThreads) cs.hist[i] = 0u;
+  // each part's candidate slot (64-bit divisions) needs nothing the previous
+  // grid writes: worked out while it finishes; thread p reads it back below
+  if (v.mode != 0)
+    for (int p = threadIdx.x; p < nparts; p += kClThreads) slot_of[p] = cand_slot(sp, seg, p);
   grid_dep_wait();   // the scores or candidate lists come from the previous grid
   grid_dep_launch();
   // list lengths and their exclusive prefix (mode 1), else the dense range
@@ -284,9 +294,7 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
       const int p = p0 + threadIdx.x;
       int len = 0;
       if (p < nparts) {
-        // each part's slot is worked out once here (it takes 64-bit divisions)
-        const int64_t slot = cand_slot(sp, seg, p);
-        slot_of[p] = slot;
+        const int64_t slot = slot_of[p];
         len = slot < 0 ? 0 : min(max(v.cand_cnt[slot], 0), v.cap);
       }
       int tot;
@@ -459,6 +467,9 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
     }
   }
   __syncthreads();
+  // no CTA reads another's shared memory after this point; a CTA may leave
+  // once every CTA of the cluster has arrived here (the wait is at the end)
+  cluster_arrive();
 
   const int n_take = mode == 0 ? 0 : mode == 2 ? E : n_sel;
   int32_t* out = idx + (size_t)b * sp.T + sp.off[h];
@@ -488,8 +499,7 @@ kvc_select_kernel(SegView v, const __grid_constant__ SelParams sp, int stage_cap
       eq_seen += __popc(eqb);
     }
   }
-  // no CTA leaves while another may still read its shared memory
-  cluster_sync_all();
+  cluster_wait();
 }
 
 // Gather retained rows: one 16-byte vector per lane, D/8 lanes per row.
