@@ -28,8 +28,9 @@ Readings taken where the page leaves a step open:
 Functions and their pins (tests/test_oracle_rawdot.py):
   summed_query: the fp64 window/group sum of raw logits (through
       kvc_oracle.dense_logits) outside the causal band.
-  quantize_int8: a hand-worked example, extremes at +-127, zero rows, and
-      the rounding error bound.
+  quantize_int8: a hand-worked example, a hand-worked row of exact .5 ties
+      (round half to even), extremes at +-127, zero rows, and the rounding
+      error bound.
   raw_scores_exact / raw_scores_int8: the analytic quantisation error bound;
       for one query (G = W = 1) the exact raw ranking equals the softmax
       oracle's selection (HillInfer's monotonicity argument).

@@ -98,3 +98,12 @@ def test_row_batched_scores_equal_the_per_key_ones():
     a = R.raw_scores_int8(q, k)
     b = R.raw_scores_int8_rows(q, k)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_round_half_to_even_hand_case(golden_dir):
+    # a row whose amax is 127 maps every element to itself, so each
+    # fractional .5 is an exact tie; the codes were worked out by hand
+    g = json.load(open(os.path.join(golden_dir, "int8_rounding_ties.json")))
+    codes, scale = R.quantize_int8(np.array(g["x"], dtype=np.float32))
+    assert codes.tolist() == g["codes"]
+    assert scale == np.float32(g["scale"])
