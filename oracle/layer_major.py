@@ -18,7 +18,9 @@ kvc_oracle.retained_layout describes for every batch element in turn.
 Pins (tests/test_oracle_layer_major.py): chunks reassemble the prompt for
 ragged and exact splits; the cache size at TideKV's main setting is the
 512 MiB of its Fig. 5 / Tables 6 and 9; per-layer rows follow
-kvc_oracle.retained_layout.
+kvc_oracle.retained_layout; budgets_pyramid matches hand-worked ramps (a
+fractional one, a remainder tie) and stays within one key of the exact
+rational ramp.
 """
 
 from __future__ import annotations

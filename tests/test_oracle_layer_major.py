@@ -45,3 +45,25 @@ def test_pyramid_budgets_sum_ends_and_shape(N, budget, k_min):
         assert abs(b[0] - (2 * budget - k_min)) <= 1 and abs(b[-1] - k_min) <= 1
     if k_min == budget:
         assert b == [budget] * N                                    # no ramp: flat
+
+
+@pytest.mark.parametrize("N,budget,k_min,expected", [
+    # worked by hand from the reading (a linear ramp from 2*budget - k_min down
+    # to k_min, largest-remainder rounding, equal remainders to the lower layer):
+    (2, 10, 3, [17, 3]),            # ends only
+    (4, 10, 1, [19, 13, 7, 1]),     # integer steps of 6
+    (4, 5, 0, [10, 7, 3, 0]),       # 10, 6.67, 3.33, 0: the one spare key goes to the largest remainder
+    (5, 4, 1, [7, 6, 4, 2, 1]),     # 7, 5.5, 4, 2.5, 1: remainders tie at layers 1 and 3, the lower one wins
+])
+def test_pyramid_budgets_hand_cases(N, budget, k_min, expected):
+    assert LM.budgets_pyramid(N, budget, k_min) == expected
+
+
+@pytest.mark.parametrize("N,budget,k_min", [(32, 4096, 1024), (48, 256, 36), (9, 100, 7), (40, 1024, 0)])
+def test_pyramid_budgets_stay_within_one_key_of_the_linear_ramp(N, budget, k_min):
+    from fractions import Fraction
+    b = LM.budgets_pyramid(N, budget, k_min)
+    k_max = 2 * budget - k_min
+    for l, x in enumerate(b):
+        exact = Fraction(k_max) - Fraction((k_max - k_min) * l, N - 1)
+        assert abs(Fraction(x) - exact) < 1
