@@ -542,6 +542,9 @@ int kvc_cache_layout(int N, int B, int H_kv, int S, const int32_t* K_l, int64_t*
 int kvc_budget_pyramid(int N, int budget, int k_min, int32_t* K_l_out) {
   if (N < 1 || !K_l_out) return set_error(KVC_ERR_INVALID_ARG, "need N >= 1 and an output array");
   if (k_min < 0 || k_min > budget) return set_error(KVC_ERR_INVALID_ARG, "need 0 <= k_min <= budget");
+  if (2 * (int64_t)budget - k_min > INT32_MAX)
+    return set_error(KVC_ERR_INVALID_ARG, "first-layer budget 2*budget - k_min = %lld does not fit int32",
+                     (long long)(2 * (int64_t)budget - k_min));
   if (N == 1) {
     K_l_out[0] = budget;
     return KVC_OK;
@@ -574,11 +577,17 @@ int kvc_budget_inverse_stability(int H_kv, const double* s_stable, int64_t total
     if (!(s_stable[h] > 0.0)) return set_error(KVC_ERR_INVALID_ARG, "stability score %d must be > 0", h);
     w[h] = 1.0 / s_stable[h];
     wsum += w[h];
+    if (!std::isfinite(w[h]) || !std::isfinite(wsum))
+      return set_error(KVC_ERR_INVALID_ARG, "stability score %d = %g: the inverse weights overflow fp64", h,
+                       s_stable[h]);
   }
   std::vector<int64_t> base(H_kv);
   int64_t assigned = 0;
   for (int h = 0; h < H_kv; ++h) {
     exact[h] = (double)total * w[h] / wsum;
+    if (!std::isfinite(exact[h]))
+      return set_error(KVC_ERR_INVALID_ARG, "share of head %d overflows fp64 (total %lld, s = %g)", h,
+                       (long long)total, s_stable[h]);
     base[h] = (int64_t)std::floor(exact[h]);
     rem[h] = exact[h] - (double)base[h];
     assigned += base[h];

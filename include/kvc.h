@@ -357,7 +357,9 @@ int kvc_cache_layout(int N, int B, int H_kv, int S, const int32_t* K_l,
  * a linear ramp from k_max = 2*budget - k_min at layer 0 down to k_min at
  * layer N-1 (mean = budget), rounded by largest remainder (ties to the
  * lower layer) so that the layers sum to exactly N * budget.
- *   K_l_out HOST [N]; 0 <= k_min <= budget.  N = 1 gives budget.
+ *   K_l_out HOST [N]; 0 <= k_min <= budget, and the first layer's
+ *   2*budget - k_min must fit int32 (else KVC_ERR_INVALID_ARG).  N = 1 gives
+ *   budget.
  */
 int kvc_budget_pyramid(int N, int budget, int k_min, int32_t* K_l_out);
 
@@ -386,6 +388,9 @@ int kvc_scan_ranges(int BH, int S, int P, int64_t* starts);
  * proportional to w_h = 1 / s_h.  The exact shares total * w_h / sum(w) are
  * rounded by largest remainder (ties to the lower head index) so that they
  * sum to `total`, then clamped to [lo, hi].  s_stable HOST [H_kv], > 0.
+ * Scores so small that 1/s, the sum of the weights or a share overflows
+ * fp64 are rejected with KVC_ERR_INVALID_ARG (the device variant does not
+ * check this and leaves such budgets unspecified).
  */
 int kvc_budget_inverse_stability(int H_kv, const double* s_stable,
                                  int64_t total, int lo, int hi,

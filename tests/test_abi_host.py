@@ -263,3 +263,20 @@ def test_scan_ranges_rejects_bad_sizes(K):
     for args in ((0, 10, 1), (1, 0, 1), (1, 10, 0)):
         with pytest.raises(K.KvcError):
             K.kvc_scan_ranges(*args)
+
+
+def test_budget_helpers_reject_overflowing_inputs(K):
+    # a first-layer budget 2*budget - k_min past int32 cannot be returned
+    with pytest.raises(K.KvcError) as ei:
+        K.kvc_budget_pyramid(4, 2**31 - 2, 0)
+    assert ei.value.code == K.KVC_ERR_INVALID_ARG
+    assert K.kvc_budget_pyramid(2, 2**30, 1) == [2**31 - 1, 1]        # the largest that fits
+    # a positive but subnormal stability score makes 1/s overflow fp64
+    for s in ([1.0, 1e-310], [1e-308, 1e-308], [1e-300, 1.0]):
+        with pytest.raises(K.KvcError) as ei:
+            K.kvc_budget_inverse_stability(s, 10**12 if s[0] == 1e-300 else 100, 0, 1 << 30)
+        assert ei.value.code == K.KVC_ERR_INVALID_ARG
+    # tiny but representable scores still work and match the oracle
+    s = [1e-200, 1.0, 2.0]
+    assert K.kvc_budget_inverse_stability(s, 1000, 0, 1 << 30) == \
+        O.budgets_inverse_stability(s, 1000, 0, 1 << 30).tolist()
