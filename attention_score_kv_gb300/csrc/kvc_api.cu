@@ -182,6 +182,8 @@ int check_shapes(int B, int H_q, int H_kv, int S, int D, int W) {
 
 int check_bs(int b_s) {
   if (b_s < kTile) return set_error(KVC_ERR_INVALID_ARG, "b_s=%d must be >= %d", b_s, kTile);
+  // the candidate capacity K_l_max + b_s (K_l_max <= S <= 2^30) stays an int
+  if (b_s > (1 << 29)) return set_error(KVC_ERR_UNSUPPORTED, "b_s=%d above 2^29", b_s);
   return KVC_OK;
 }
 
@@ -364,6 +366,8 @@ size_t kvc_workspace_size(int B, int H_q, int H_kv, int D, int W, int b_s, int K
     set_error(KVC_ERR_INVALID_ARG, "K_l_max must be >= 0");
     return 0;
   }
+  // a budget above S keeps min(K_l, S) rows, and S <= 2^30
+  K_l_max = std::min(K_l_max, 1 << 30);
   WsLayout L;
   if (!layout_ws(B, H_q, H_kv, D, W, b_s, K_l_max, pool_k, -1, &L)) {
     set_error(KVC_ERR_CUDA, "no CUDA device to size the workspace for");

@@ -70,6 +70,7 @@ int kvc_version(void);
  * current device.  There is no S argument: the scan keeps only W-length
  * normaliser state per key range and, per key range, at most K_l_max + b_s
  * candidate keys (TideKV Fig. 3: Temp = O(W b_s + K_l), independent of S).
+ * 128 <= b_s <= 2^29; K_l_max above 2^30 (the largest S) sizes as 2^30.
  * Returns 0 and sets kvc_last_error() on invalid sizes or without a device.
  */
 size_t kvc_workspace_size(int B, int H_q, int H_kv, int D, int W, int b_s,
@@ -83,7 +84,7 @@ size_t kvc_workspace_size(int B, int H_q, int H_kv, int D, int W, int b_s,
  *   k     [B, H_kv, S, D] bf16  the layer's prefix keys
  *   m     [B, H_q, W] fp32 out  m = max_{j <= t_i} q.k_j / sqrt(D)
  *   Z     [B, H_q, W] fp32 out  Z = sum_{j <= t_i} exp(q.k_j / sqrt(D) - m)
- * b_s must be >= 128.
+ * b_s must be >= 128 and <= 2^29 (KVC_ERR_UNSUPPORTED above).
  */
 int kvc_score_pass1(const kvc_bf16* q_win, const kvc_bf16* k, int B, int H_q,
                     int H_kv, int S, int D, int W, int b_s, float* m, float* Z,

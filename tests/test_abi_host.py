@@ -280,3 +280,13 @@ def test_budget_helpers_reject_overflowing_inputs(K):
     s = [1e-200, 1.0, 2.0]
     assert K.kvc_budget_inverse_stability(s, 1000, 0, 1 << 30) == \
         O.budgets_inverse_stability(s, 1000, 0, 1 << 30).tolist()
+
+
+def test_workspace_rejects_a_key_block_that_would_overflow_the_candidate_capacity(K):
+    # checked before the device is asked for its SM count, so no GPU is needed
+    with pytest.raises(K.KvcError) as ei:
+        K.kvc_workspace_size(1, 4, 2, 64, 16, 2**29 + 1, 100, 1)
+    assert "b_s" in str(ei.value)
+    with pytest.raises(K.KvcError) as ei:
+        K.kvc_workspace_size(1, 4, 2, 64, 16, 127, 100, 1)
+    assert "b_s" in str(ei.value)
